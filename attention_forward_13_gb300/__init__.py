@@ -1,0 +1,225 @@
+"""GB300 (sm_103a) fused attention forward: thin Python binding of the C ABI.
+
+Every function here only marshals torch tensors (device pointers, sizes,
+strides, the current CUDA stream) into the C library ``libattn_fwd.so``; all
+arithmetic runs in the library's CUDA kernels.  There is no fallback: if the
+library is missing and cannot be built, or a call fails, an exception is
+raised.  Output tensors are allocated with torch when not given.
+
+    o, lse = attn_fwd(q, k, v, causal=True)                 # [B,H,L,d]
+    o, lse = attn_fwd_varlen(q, k, v, cu_q, cu_k, max_q)    # [total,H,d]
+    o, lse = attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k)
+    o, lse = attn_splitkv_combine(o_part, lse_part)
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+__all__ = ["attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_splitkv_combine",
+           "attn_paged_workspace_bytes", "attn_paged_auto_splits", "attn_device_error",
+           "attn_selftest_timeout", "attn_last_kernel_name", "AttnError", "library"]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, fn: str):
+        self.status = status
+        super().__init__(f"{fn}: {_lib.STATUS.get(status, status)}")
+
+
+def library() -> ctypes.CDLL:
+    return _lib.load()
+
+
+def _check(status: int, fn: str):
+    if status != 0:
+        raise AttnError(status, fn)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.ATTN_BF16
+    if t.dtype == torch.float16:
+        return _lib.ATTN_F16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _opts(scale, causal, softcap, sink):
+    o = _lib.attn_opts()
+    o.scale = float(scale) if scale is not None else 0.0
+    o.causal = 1 if causal else 0
+    o.softcap = float(softcap) if softcap else 0.0
+    o.sink = sink.data_ptr() if sink is not None else None
+    return o
+
+
+def _strides_bhld(t):
+    s = t.stride()
+    if s[3] != 1:
+        raise ValueError("innermost (head-dim) stride must be 1")
+    return _lib.attn_strides(s[0], s[1], s[2])
+
+
+def _strides_thd(t):
+    s = t.stride()
+    if s[2] != 1:
+        raise ValueError("innermost (head-dim) stride must be 1")
+    return _lib.attn_strides(0, s[1], s[0])
+
+
+def _check_sink(sink, Hq, device):
+    if sink is None:
+        return None
+    if sink.dtype != torch.float32 or sink.numel() != Hq or sink.device != device:
+        raise ValueError("sink must be fp32 [Hq] on the same device")
+    return sink.contiguous()
+
+
+def attn_fwd(q, k, v, o=None, lse=True, causal=False, scale=None, softcap=0.0, sink=None,
+             stream=None):
+    """Dense attention.  q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] (any strides with d-stride 1).
+    Returns (o [B,Hq,Lq,d], lse fp32 [B,Hq,Lq] or None)."""
+    B, Hq, Lq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if o is None:
+        o = torch.empty((B, Hq, Lq, d), dtype=q.dtype, device=q.device)
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+    sink = _check_sink(sink, Hq, q.device)
+    opts = _opts(scale, causal, softcap, sink)
+    st = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, Hq, Hkv, Lq, Lk,
+                            d, _dtype_code(q), _strides_bhld(q), _strides_bhld(k),
+                            _strides_bhld(v), _strides_bhld(o), ctypes.byref(opts),
+                            _stream(stream))
+    _check(st, "attn_fwd")
+    return o, lse_t
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, o=None, lse=True,
+                    causal=False, scale=None, softcap=0.0, sink=None, stream=None):
+    """Group mode.  q [total_q,Hq,d], k/v [total_k,Hkv,d], cu_seqlens int32 [B+1] on the
+    device.  Returns (o [total_q,Hq,d], lse fp32 [Hq,total_q] or None)."""
+    total_q, Hq, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    for cu in (cu_seqlens_q, cu_seqlens_k):
+        if cu.dtype != torch.int32 or cu.device != q.device or not cu.is_contiguous():
+            raise ValueError("cu_seqlens must be contiguous int32 on the device")
+    if o is None:
+        o = torch.empty((total_q, Hq, d), dtype=q.dtype, device=q.device)
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+    sink = _check_sink(sink, Hq, q.device)
+    opts = _opts(scale, causal, softcap, sink)
+    st = library().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t),
+                                   _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, total_q, total_k,
+                                   int(max_seqlen_q), Hq, Hkv, d, _dtype_code(q),
+                                   _strides_thd(q), _strides_thd(k), _strides_thd(v),
+                                   _strides_thd(o), ctypes.byref(opts), _stream(stream))
+    _check(st, "attn_fwd_varlen")
+    return o, lse_t
+
+
+def attn_paged_workspace_bytes(B, Lq, Hq, d, num_splits) -> int:
+    return int(library().attn_paged_workspace_bytes(B, Lq, Hq, d, num_splits))
+
+
+def attn_paged_auto_splits(B, Hkv, max_pages_per_seq) -> int:
+    return int(library().attn_paged_auto_splits(B, Hkv, max_pages_per_seq))
+
+
+def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=None, lse=True,
+                   causal=False, scale=None, softcap=0.0, sink=None, workspace=None,
+                   stream=None):
+    """Paged KV.  q [B,Lq,Hq,d], pools [num_pages,page,Hkv,d], block_table int32
+    [B,max_pages], seqlens_k int32 [B] (all on the device, contiguous).
+    Returns (o [B,Lq,Hq,d], lse fp32 [B,Hq,Lq] or None)."""
+    B, Lq, Hq, d = q.shape
+    num_pages, page, Hkv, _ = k_pool.shape
+    max_pages = block_table.shape[1]
+    for t in (q, k_pool, v_pool, block_table, seqlens_k):
+        if not t.is_contiguous():
+            raise ValueError("paged inputs must be contiguous")
+    if num_splits == 0:
+        num_splits = attn_paged_auto_splits(B, Hkv, max_pages)
+    if o is None:
+        o = torch.empty((B, Lq, Hq, d), dtype=q.dtype, device=q.device)
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+    o_part = lse_part = None
+    if num_splits > 1:
+        rows = B * Hq * Lq
+        need = num_splits * rows * (d + 1)
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.empty(need, dtype=torch.float32, device=q.device)
+        o_part = workspace[: num_splits * rows * d]
+        lse_part = workspace[num_splits * rows * d: need]
+    sink = _check_sink(sink, Hq, q.device)
+    opts = _opts(scale, causal, softcap, sink)
+    st = library().attn_fwd_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                  _ptr(seqlens_k), _ptr(o), _ptr(lse_t), B, Lq, Hq, Hkv, d,
+                                  _dtype_code(q), page, num_pages, max_pages, num_splits,
+                                  _ptr(o_part), _ptr(lse_part), ctypes.byref(opts),
+                                  _stream(stream))
+    _check(st, "attn_fwd_paged")
+    return o, lse_t
+
+
+def attn_splitkv_combine(o_partial, lse_partial, sink=None, dtype=torch.bfloat16, o=None,
+                         lse=True, stream=None):
+    """Merge split partials.  o_partial fp32 [S,B,Hq,Lq,d], lse_partial fp32 [S,B,Hq,Lq].
+    Returns (o [B,Lq,Hq,d] in ``dtype``, lse fp32 [B,Hq,Lq] or None)."""
+    S, B, Hq, Lq, d = o_partial.shape
+    if o is None:
+        o = torch.empty((B, Lq, Hq, d), dtype=dtype, device=o_partial.device)
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((B, Hq, Lq), dtype=torch.float32, device=o_partial.device)
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+    sink = _check_sink(sink, Hq, o_partial.device)
+    st = library().attn_splitkv_combine(_ptr(o_partial.contiguous()),
+                                        _ptr(lse_partial.contiguous()), S, B, Hq, Lq, d,
+                                        _ptr(sink), _ptr(o), _dtype_code(o), _ptr(lse_t),
+                                        _stream(stream))
+    _check(st, "attn_splitkv_combine")
+    return o, lse_t
+
+
+def attn_device_error() -> int:
+    """Synchronises, reads and clears the device error word; returns its bits."""
+    bits = ctypes.c_uint(0)
+    st = library().attn_device_error(ctypes.byref(bits))
+    if st not in (0, 4):
+        raise AttnError(st, "attn_device_error")
+    return int(bits.value)
+
+
+def attn_selftest_timeout(timeout_ns: int, stream=None) -> None:
+    _check(library().attn_selftest_timeout(int(timeout_ns), _stream(stream)),
+           "attn_selftest_timeout")
+
+
+def attn_last_kernel_name() -> str:
+    return library().attn_last_kernel_name().decode()

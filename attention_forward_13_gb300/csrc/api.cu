@@ -1,0 +1,463 @@
+// api.cu -- the C ABI declared in include/attn_fwd.h: argument validation,
+// TMA descriptor encoding, split selection and kernel dispatch.  No device
+// memory is allocated here; every launch is asynchronous on the caller's
+// stream.
+#include "../../include/attn_fwd.h"
+#include "common.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+using namespace attn;
+
+namespace {
+
+// Device error word: one per device, set by kernels that give up on a wait.
+__device__ unsigned int g_attn_err;
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+std::mutex g_mu;
+
+thread_local char g_last_name[160] = "";
+
+// Default limit of every in-kernel wait: generous for any legal schedule, and
+// still a bounded time if a schedule is ever wrong.
+constexpr uint64_t kTimeoutNs = 4ull * 1000000000ull;
+
+bool log_enabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("ATTN_LOG");
+    v = (e != nullptr && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
+
+attn_status device_state(unsigned int** err, int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_attn_err) != cudaSuccess) return ATTN_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<unsigned int*>(ptr);
+    g_num_sms[dev] = sms;
+  }
+  if (err) *err = g_err_ptr[dev];
+  if (num_sms) *num_sms = g_num_sms[dev];
+  return ATTN_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// Tiled map over a tensor whose innermost dimension is d (contiguous) and
+// whose other dimensions have the given extents and byte strides; the box is
+// 64 elements (128 bytes, one swizzle atom) by box[1..].
+bool make_map(CUtensorMap* m, const void* base, bool bf16, int rank, const uint64_t* dims,
+              const uint64_t* strides_bytes, const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  memset(m, 0, sizeof(*m));
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  rank, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool stride_ok(int64_t s) { return s > 0 && (s % 8) == 0; }
+
+float resolve_scale(const attn_opts* o, int d) {
+  return (o != nullptr && o->scale > 0.0f) ? o->scale : 1.0f / sqrtf(static_cast<float>(d));
+}
+
+void fill_common(PrefillParams& p, const attn_opts* opts, int d) {
+  const float scale = resolve_scale(opts, d);
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  const float cap = (opts != nullptr && opts->softcap > 0.0f) ? opts->softcap : 0.0f;
+  p.softcap = cap;
+  p.softcap_inv = cap > 0.0f ? 1.0f / cap : 0.0f;
+  p.sink = opts != nullptr ? opts->sink : nullptr;
+  p.timeout_ns = kTimeoutNs;
+}
+
+attn_status finish_launch(cudaError_t e) {
+  if (e != cudaSuccess) {
+    if (log_enabled()) fprintf(stderr, "[attn] launch failed: %s\n", cudaGetErrorString(e));
+    return ATTN_ERR_CUDA;
+  }
+  if (log_enabled()) fprintf(stderr, "[attn] launched %s\n", g_last_name);
+  return ATTN_OK;
+}
+
+__global__ void attn_selftest_timeout_kernel(unsigned int* err, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const Waiter w{globaltimer_ns() + timeout_ns, &abort_flag, err};
+  // Nobody ever arrives on `bar`: the bounded wait must give up and return.
+  w.wait(&bar, 0, kErrSelftest);
+  __syncthreads();
+}
+
+}  // namespace
+
+namespace attn {
+cudaError_t launch_selftest_timeout(unsigned int* err, unsigned long long timeout_ns,
+                                    cudaStream_t stream) {
+  attn_selftest_timeout_kernel<<<1, 32, 0, stream>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
+}  // namespace attn
+
+extern "C" {
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* attn_last_kernel_name(void) { return g_last_name; }
+
+attn_status attn_device_error(unsigned int* bits) {
+  unsigned int* err = nullptr;
+  attn_status st = device_state(&err, nullptr);
+  if (st != ATTN_OK) return st;
+  unsigned int h = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemcpy(&h, err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (h != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  if (bits) *bits = h;
+  return h ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+attn_status attn_selftest_timeout(uint64_t timeout_ns, void* stream) {
+  unsigned int* err = nullptr;
+  attn_status st = device_state(&err, nullptr);
+  if (st != ATTN_OK) return st;
+  if (timeout_ns == 0 || timeout_ns > 10ull * 1000000000ull) return ATTN_ERR_INVALID;
+  snprintf(g_last_name, sizeof(g_last_name), "attn_selftest_timeout");
+  return finish_launch(
+      launch_selftest_timeout(err, timeout_ns, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int Lq, int Lk, int d, attn_dtype dtype, attn_strides sq,
+                     attn_strides sk, attn_strides sv, attn_strides so, const attn_opts* opts,
+                     void* stream) {
+  if (B < 0 || Lq < 0 || Lk < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Lq == 0) return ATTN_OK;
+  // With Lk = 0 nothing of K/V is read and they may be NULL.
+  if (q == nullptr || o == nullptr || (Lk > 0 && (k == nullptr || v == nullptr)))
+    return ATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return ATTN_ERR_INVALID;
+  for (const attn_strides* s : {&sq, &sk, &sv, &so})
+    if (!stride_ok(s->row) || !stride_ok(s->head) || !stride_ok(s->batch)) return ATTN_ERR_INVALID;
+  if (opts != nullptr && opts->sink != nullptr && (reinterpret_cast<uintptr_t>(opts->sink) & 3u))
+    return ATTN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * Hq * ((Lq + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+
+  PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  unsigned int* err = nullptr;
+  if (device_state(&err, nullptr) != ATTN_OK) return ATTN_ERR_CUDA;
+  const bool bf16 = dtype == ATTN_BF16;
+  const uint32_t box[4] = {64, 128, 1, 1};
+  {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lq, (uint64_t)Hq, (uint64_t)B};
+    const uint64_t st[3] = {(uint64_t)sq.row * 2, (uint64_t)sq.head * 2, (uint64_t)sq.batch * 2};
+    if (!make_map(&p.tm_q, q, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+  }
+  if (Lk > 0) {  // Lk = 0: no key tile is ever loaded, the maps stay unused
+    {
+      const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lk, (uint64_t)Hkv, (uint64_t)B};
+      const uint64_t st[3] = {(uint64_t)sk.row * 2, (uint64_t)sk.head * 2,
+                              (uint64_t)sk.batch * 2};
+      if (!make_map(&p.tm_k, k, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+    }
+    {
+      const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lk, (uint64_t)Hkv, (uint64_t)B};
+      const uint64_t st[3] = {(uint64_t)sv.row * 2, (uint64_t)sv.head * 2,
+                              (uint64_t)sv.batch * 2};
+      if (!make_map(&p.tm_v, v, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+    }
+  }
+  p.o = o;
+  p.lse = lse;
+  p.o_row = so.row;
+  p.o_head = so.head;
+  p.o_batch = so.batch;
+  p.lse_head = Lq;
+  p.lse_batch = static_cast<int64_t>(Hq) * Lq;
+  p.cu_q = p.cu_k = nullptr;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.num_m_blocks = (Lq + 255) / 256;
+  p.err = err;
+  fill_common(p, opts, d);
+  const bool causal = opts != nullptr && opts->causal != 0;
+  const int grid = p.num_m_blocks * B * Hq;
+  return finish_launch(launch_prefill(p, grid, d, bf16, causal, p.softcap > 0.0f,
+                                      static_cast<cudaStream_t>(stream), g_last_name,
+                                      sizeof(g_last_name)));
+}
+
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B,
+                            int total_q, int total_k, int max_seqlen_q, int Hq, int Hkv, int d,
+                            attn_dtype dtype, attn_strides sq, attn_strides sk, attn_strides sv,
+                            attn_strides so, const attn_opts* opts, void* stream) {
+  if (B < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || Hq <= 0 || Hkv <= 0 ||
+      Hq % Hkv != 0)
+    return ATTN_ERR_INVALID;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || total_q == 0 || max_seqlen_q == 0) return ATTN_OK;
+  if (q == nullptr || o == nullptr || cu_seqlens_q == nullptr || cu_seqlens_k == nullptr ||
+      (total_k > 0 && (k == nullptr || v == nullptr)))
+    return ATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return ATTN_ERR_INVALID;
+  for (const attn_strides* s : {&sq, &sk, &sv, &so})
+    if (!stride_ok(s->row) || !stride_ok(s->head)) return ATTN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * Hq * ((max_seqlen_q + 255) / 256) > 0x7fffffffLL)
+    return ATTN_ERR_UNSUPPORTED;
+
+  PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  unsigned int* err = nullptr;
+  if (device_state(&err, nullptr) != ATTN_OK) return ATTN_ERR_CUDA;
+  const bool bf16 = dtype == ATTN_BF16;
+  const uint32_t box[4] = {64, 128, 1, 1};
+  {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)total_q, (uint64_t)Hq, 1};
+    const uint64_t st[3] = {(uint64_t)sq.row * 2, (uint64_t)sq.head * 2,
+                            (uint64_t)sq.row * 2 * (uint64_t)total_q};
+    if (!make_map(&p.tm_q, q, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+  }
+  if (total_k > 0) {  // no keys at all: the maps stay unused
+    const int tk = total_k;
+    {
+      const uint64_t dims[4] = {(uint64_t)d, (uint64_t)tk, (uint64_t)Hkv, 1};
+      const uint64_t st[3] = {(uint64_t)sk.row * 2, (uint64_t)sk.head * 2,
+                              (uint64_t)sk.row * 2 * (uint64_t)tk};
+      if (!make_map(&p.tm_k, k, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+    }
+    {
+      const uint64_t dims[4] = {(uint64_t)d, (uint64_t)tk, (uint64_t)Hkv, 1};
+      const uint64_t st[3] = {(uint64_t)sv.row * 2, (uint64_t)sv.head * 2,
+                              (uint64_t)sv.row * 2 * (uint64_t)tk};
+      if (!make_map(&p.tm_v, v, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+    }
+  }
+  p.o = o;
+  p.lse = lse;
+  p.o_row = so.row;
+  p.o_head = so.head;
+  p.o_batch = 0;
+  p.lse_head = total_q;
+  p.lse_batch = 0;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lq = 0;
+  p.Lk = 0;
+  p.num_m_blocks = (max_seqlen_q + 255) / 256;
+  p.err = err;
+  fill_common(p, opts, d);
+  const bool causal = opts != nullptr && opts->causal != 0;
+  const int grid = p.num_m_blocks * B * Hq;
+  return finish_launch(launch_prefill(p, grid, d, bf16, causal, p.softcap > 0.0f,
+                                      static_cast<cudaStream_t>(stream), g_last_name,
+                                      sizeof(g_last_name)));
+}
+
+size_t attn_paged_workspace_bytes(int B, int Lq, int Hq, int d, int num_splits) {
+  if (B <= 0 || Lq <= 0 || Hq <= 0 || d <= 0 || num_splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * Lq;
+  return static_cast<size_t>(num_splits) * rows * (static_cast<size_t>(d) + 1) * sizeof(float);
+}
+
+int attn_paged_auto_splits(int B, int Hkv, int max_pages_per_seq) {
+  int sms = 148;
+  device_state(nullptr, &sms);
+  if (B <= 0 || Hkv <= 0 || max_pages_per_seq <= 0) return 1;
+  // Aim for about two resident CTAs per SM worth of (sequence, kv head, split)
+  // work items, but never fewer than ~8 pages (512 keys at page 64) per split.
+  const int64_t pairs = static_cast<int64_t>(B) * Hkv;
+  int64_t want = (4LL * sms + pairs - 1) / pairs;
+  const int64_t max_useful = (max_pages_per_seq + 7) / 8;
+  if (want > max_useful) want = max_useful;
+  if (want < 1) want = 1;
+  if (want > 64) want = 64;
+  return static_cast<int>(want);
+}
+
+attn_status attn_splitkv_combine(const float* o_partial, const float* lse_partial,
+                                 int num_splits, int B, int Hq, int Lq, int d,
+                                 const float* sink, void* o, attn_dtype dtype, float* lse,
+                                 void* stream) {
+  if (num_splits < 1 || num_splits > 64 || B < 0 || Hq <= 0 || Lq < 0) return ATTN_ERR_INVALID;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Lq == 0) return ATTN_OK;
+  if (o_partial == nullptr || lse_partial == nullptr || o == nullptr) return ATTN_ERR_INVALID;
+  if (!aligned16(o_partial) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse_partial) & 3u) ||
+      (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return ATTN_ERR_INVALID;
+  CombineParams c;
+  c.o_part = o_partial;
+  c.lse_part = lse_partial;
+  c.sink = sink;
+  c.o = o;
+  c.lse = lse;
+  c.num_splits = num_splits;
+  c.B = B;
+  c.Hq = Hq;
+  c.Lq = Lq;
+  c.d = d;
+  return finish_launch(launch_combine(c, dtype == ATTN_BF16, static_cast<cudaStream_t>(stream),
+                                      g_last_name, sizeof(g_last_name)));
+}
+
+attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_table, const int32_t* seqlens_k, void* o,
+                           float* lse, int B, int Lq, int Hq, int Hkv, int d, attn_dtype dtype,
+                           int page_size, int num_pages, int max_pages_per_seq, int num_splits,
+                           float* o_partial, float* lse_partial, const attn_opts* opts,
+                           void* stream) {
+  if (B < 0 || Lq < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_pages <= 0 ||
+      max_pages_per_seq <= 0 || num_splits < 0 || num_splits > 64)
+    return ATTN_ERR_INVALID;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128 &&
+      page_size != 256)
+    return ATTN_ERR_UNSUPPORTED;
+  if (Lq * (Hq / Hkv) > 16) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_pages) * page_size > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Lq == 0) return ATTN_OK;
+  if (q == nullptr || k_pool == nullptr || v_pool == nullptr || block_table == nullptr ||
+      seqlens_k == nullptr || o == nullptr)
+    return ATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) ||
+      (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return ATTN_ERR_INVALID;
+  if (B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (num_splits == 0) num_splits = attn_paged_auto_splits(B, Hkv, max_pages_per_seq);
+  if (num_splits > 1 && (o_partial == nullptr || lse_partial == nullptr ||
+                         !aligned16(o_partial) || (reinterpret_cast<uintptr_t>(lse_partial) & 3u)))
+    return ATTN_ERR_INVALID;
+
+  DecodeParams p;
+  memset(&p, 0, sizeof(p));
+  unsigned int* err = nullptr;
+  if (device_state(&err, nullptr) != ATTN_OK) return ATTN_ERR_CUDA;
+  const bool bf16 = dtype == ATTN_BF16;
+  const uint32_t box[3] = {64, (uint32_t)(page_size < 128 ? page_size : 128), 1};
+  const uint32_t boxr[3] = {64, 1, box[1]};
+  (void)box;
+  const uint64_t dims[3] = {(uint64_t)d, (uint64_t)Hkv, (uint64_t)num_pages * page_size};
+  const uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)Hkv * d * 2};
+  if (!make_map(&p.tm_k, k_pool, bf16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
+  if (!make_map(&p.tm_v, v_pool, bf16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
+  p.q = q;
+  p.block_table = block_table;
+  p.seqlens_k = seqlens_k;
+  p.o = o;
+  p.lse = lse;
+  p.o_part = o_partial;
+  p.lse_part = o_partial != nullptr && num_splits > 1 ? lse_partial : nullptr;
+  p.sink = opts != nullptr ? opts->sink : nullptr;
+  p.B = B;
+  p.Lq = Lq;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
+  p.max_pages = max_pages_per_seq;
+  p.num_splits = num_splits;
+  p.chunk_pages = (max_pages_per_seq + num_splits - 1) / num_splits;
+  const float scale = resolve_scale(opts, d);
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.softcap = (opts != nullptr && opts->softcap > 0.0f) ? opts->softcap : 0.0f;
+  p.softcap_inv = p.softcap > 0.0f ? 1.0f / p.softcap : 0.0f;
+  p.causal = (opts != nullptr && opts->causal != 0) ? 1 : 0;
+  p.err = err;
+  p.timeout_ns = kTimeoutNs;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  attn_status st1 = finish_launch(launch_decode(p, d, bf16, p.softcap > 0.0f, Lq * (Hq / Hkv), s,
+                                                g_last_name, sizeof(g_last_name)));
+  if (st1 != ATTN_OK || num_splits == 1) return st1;
+  return attn_splitkv_combine(o_partial, p.lse_part, num_splits, B, Hq, Lq, d, p.sink, o, dtype,
+                              lse, stream);
+}
+
+}  // extern "C"

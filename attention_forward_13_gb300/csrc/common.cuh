@@ -1,0 +1,85 @@
+// common.cuh -- parameter blocks and small device helpers shared by the
+// attention kernels of this library (prefill, paged decode, combine).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device error word bits (one per wait site / check).
+enum ErrBits : uint32_t {
+  kErrPrefillQ = 0,
+  kErrPrefillKFull = 1,
+  kErrPrefillVFull = 2,
+  kErrPrefillKEmpty = 3,
+  kErrPrefillVEmpty = 4,
+  kErrPrefillSFull = 5,
+  kErrPrefillPFull = 6,
+  kErrPrefillOFinal = 7,
+  kErrPrefillTeardown = 8,
+  kErrDecodeFull = 12,
+  kErrDecodeEmpty = 13,
+  kErrDecodeBadPage = 14,
+  kErrDecodeTeardown = 15,
+  kErrSelftest = 20,
+};
+
+// Prefill (dense / varlen) launch parameters.  Tensor maps are 4-D
+// (d, rows, heads, batch); varlen problems use one batch slot and a row base.
+struct PrefillParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  void* o;
+  float* lse;
+  int64_t o_row, o_head, o_batch;  // element strides of O
+  int64_t lse_head, lse_batch;     // element strides of LSE (row stride 1)
+  const int32_t* cu_q;             // varlen: [B+1] (nullptr in batch mode)
+  const int32_t* cu_k;
+  const float* sink;               // [Hq] or nullptr
+  int B, Hq, Hkv, Lq, Lk;          // batch-mode lengths (ignored for varlen)
+  int total_q, total_k;            // varlen: packed extents (sequences are clamped to them)
+  int num_m_blocks;                // 256-row query blocks per (b, h)
+  float scale_log2;                // scale * log2(e)
+  float scale;                     // plain scale (soft-cap path)
+  float softcap;                   // cap (> 0 when the soft-cap variant runs)
+  float softcap_inv;               // 1 / cap
+  unsigned int* err;
+  uint64_t timeout_ns;
+};
+
+// Paged split-KV decode parameters.
+struct DecodeParams {
+  CUtensorMap tm_k;  // 3-D (d, Hkv, num_pages * page_size)
+  CUtensorMap tm_v;
+  const void* q;     // [B][Lq][Hq][d]
+  const int32_t* block_table;
+  const int32_t* seqlens_k;
+  void* o;           // final O [B][Lq][Hq][d] (num_splits == 1)
+  float* lse;        // final LSE [B][Hq][Lq] or nullptr (num_splits == 1)
+  float* o_part;     // [S][B][Hq][Lq][d] (num_splits > 1)
+  float* lse_part;   // [S][B][Hq][Lq]
+  const float* sink; // [Hq] or nullptr (used only when num_splits == 1)
+  int B, Lq, Hq, Hkv, page_size, num_pages, max_pages, num_splits, chunk_pages;
+  float scale_log2, scale, softcap, softcap_inv;
+  int causal;
+  unsigned int* err;
+  uint64_t timeout_ns;
+};
+
+struct CombineParams {
+  const float* o_part;
+  const float* lse_part;
+  const float* sink;
+  void* o;
+  float* lse;
+  int num_splits, B, Hq, Lq, d;
+};
+
+}  // namespace attn

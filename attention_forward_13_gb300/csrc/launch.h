@@ -1,0 +1,23 @@
+// launch.h -- host-side launchers of the kernels (one per translation unit),
+// called by the C ABI layer in api.cu after validation.
+#pragma once
+#include <cstddef>
+#include <cuda_runtime.h>
+#include "common.cuh"
+
+namespace attn {
+
+// grid = number of CTAs; name receives the kernel's trait string.
+cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool causal,
+                           bool softcap, cudaStream_t stream, char* name, size_t name_len);
+
+cudaError_t launch_decode(const DecodeParams& p, int d, bool bf16, bool softcap, int rows,
+                          cudaStream_t stream, char* name, size_t name_len);
+
+cudaError_t launch_combine(const CombineParams& p, bool bf16, cudaStream_t stream, char* name,
+                           size_t name_len);
+
+cudaError_t launch_selftest_timeout(unsigned int* err, unsigned long long timeout_ns,
+                                    cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,475 @@
+// prefill.cu -- fused attention forward for dense and varlen (group-mode)
+// problems on sm_103a: TMA loads into 128B-swizzled shared memory behind
+// mbarrier rings, S = Q K^T and O += P V on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in tensor memory), online softmax in registers.
+//
+// Prior art on the pages: the DefTruth flash_attn_mma_share_kv_F32F16F16F32.cu
+// kernel (FlashAttention-2 with mma.sync: Q tile kept on chip, K/V tiles
+// streamed, online max/sum with the exp(m_old - m_new) rescale, final 1/l),
+// the FlashAttention-3 hopper/epilogue_fwd.hpp epilogue (one LSE writer per
+// row, predicated stores for varlen, store_zero for empty work) and the
+// Composable Kernel fmha_fwd_pagedkv_kernel.hpp prologue (group-mode offsets,
+// GQA kv head = h / ratio, heaviest causal tiles first, the scale*log2(e)
+// fold).  The Blackwell design here differs from all three:
+//
+//  * one CTA owns TWO 128-row query tiles of one (batch, head) and streams
+//    128-key K/V tiles once for both; warps 0-3 run the softmax of tile 0,
+//    warps 4-7 that of tile 1, warp 8 issues TMA, warp 9 issues tcgen05.mma.
+//    While one warpgroup computes exponentials the tensor core works on the
+//    other tile (ping-pong).
+//  * S lives in tensor memory (fp32, 128 columns per tile).  The softmax
+//    writes P (bf16/fp16) back over the first 64 columns of its S and the
+//    P.V MMA reads its A operand straight from tensor memory.
+//  * O accumulates in tensor memory.  The running max used as the exp2
+//    subtrahend is only raised when the row max grows by more than 8 (log2
+//    units); otherwise O is not rescaled.  This is exact: the final O/l and
+//    LSE use the same subtrahend.
+//  * every mbarrier wait is bounded (Waiter): a CTA that gives up records a
+//    bit in the device error word, drains its own copies and MMAs, frees its
+//    tensor memory and returns.
+#include "ptx.cuh"
+#include "common.cuh"
+#include "launch.h"
+
+#include <cstdio>
+#include <cstring>
+#include <type_traits>
+
+namespace attn {
+
+template <int D_>
+struct PrefillCfg {
+  static constexpr int D = D_;
+  static constexpr int BM = 128;                 // rows per query tile
+  static constexpr int BN = 128;                 // keys per K/V tile
+  static constexpr int NCHUNK = D / 64;          // 64-element (128-byte) swizzle atoms along d
+  static constexpr int TILE_BYTES = BN * D * 2;  // one Q, K or V tile
+  static constexpr int CHUNK_BYTES = BN * 128;   // one swizzle-atom column of a tile
+  static constexpr int NS = (D == 128) ? 2 : 3;  // K/V ring depth
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TM_COLS = 512;
+  // Tensor-memory columns: S/P of tile t at 128*t, O of tile t at 256 + D*t.
+  __device__ static constexpr uint32_t tm_s(int t) { return 128u * t; }
+  __device__ static constexpr uint32_t tm_o(int t) { return 256u + D * t; }
+};
+
+template <class C>
+struct PrefillSmem {
+  alignas(1024) uint8_t q[2][C::TILE_BYTES];
+  alignas(1024) uint8_t k[C::NS][C::TILE_BYTES];
+  alignas(1024) uint8_t v[C::NS][C::TILE_BYTES];
+  uint64_t q_full;
+  uint64_t k_full[C::NS], k_empty[C::NS], v_full[C::NS], v_empty[C::NS];
+  uint64_t s_full[2], p_full[2], o_final[2];
+  uint64_t teardown;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// tanh(y) = 1 - 2 / (exp(2y) + 1), with exp through the special-function unit.
+__device__ __forceinline__ float tanh_via_exp2(float y) {
+  const float e = ex2_approx(y * (2.0f * kLog2e));
+  return 1.0f - 2.0f * rcp_approx(e + 1.0f);
+}
+
+// Wait for a barrier phase ignoring the abort flag (teardown only).
+__device__ __forceinline__ bool wait_raw(uint64_t* bar, uint32_t parity, uint64_t deadline) {
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() > deadline) return false;
+  }
+  return true;
+}
+
+template <int D, bool BF16, bool CAUSAL, bool SOFTCAP>
+__global__ void __launch_bounds__(320, 1)
+    attn_prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using C = PrefillCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  PrefillSmem<C>& sm = *reinterpret_cast<PrefillSmem<C>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  // ---- which (query block, head, batch) this CTA owns -----------------------
+  // Causal problems run the heaviest query blocks first (Composable Kernel
+  // GetTileIndex reverses the m-tile order when masking).
+  const int nbh = p.B * p.Hq;
+  const int mb_i = blockIdx.x / nbh;
+  const int bh = blockIdx.x - mb_i * nbh;
+  const int mb = CAUSAL ? (p.num_m_blocks - 1 - mb_i) : mb_i;
+  const int h = bh % p.Hq;
+  const int b = bh / p.Hq;
+  const int hk = h / (p.Hq / p.Hkv);
+  int Lq = p.Lq, Lk = p.Lk, rq0 = 0, rk0 = 0, bcoord = b;
+  if (p.cu_q != nullptr) {  // group mode (Composable Kernel seqstart_q/k)
+    rq0 = p.cu_q[b];
+    Lq = p.cu_q[b + 1] - rq0;
+    rk0 = p.cu_k[b];
+    Lk = p.cu_k[b + 1] - rk0;
+    bcoord = 0;
+    // Sequences never reach past the packed tensors, whatever cu_seqlens holds.
+    if (rq0 < 0 || rq0 > p.total_q) Lq = 0;
+    Lq = min(Lq, p.total_q - rq0);
+    if (rk0 < 0 || rk0 > p.total_k) Lk = 0;
+    Lk = max(0, min(Lk, p.total_k - rk0));
+  }
+  const int m0 = mb * 2 * C::BM;
+  if (m0 >= Lq) return;  // uniform early exit, nothing set up yet
+
+  // KV tiles each query tile needs.
+  int n_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int mt = m0 + t * C::BM;
+    if (mt >= Lq) {
+      n_t[t] = 0;
+    } else {
+      const int last = min(mt + C::BM - 1, Lq - 1);
+      const int kend = CAUSAL ? min(Lk, last + (Lk - Lq) + 1) : Lk;
+      n_t[t] = kend > 0 ? (kend + C::BN - 1) / C::BN : 0;
+    }
+  }
+  const int n_max = max(n_t[0], n_t[1]);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t], 128);
+      mbar_init(&sm.o_final[t], 1);
+    }
+    mbar_init(&sm.teardown, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&sm.tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const Waiter w{globaltimer_ns() + p.timeout_ns, &sm.abort_flag, p.err};
+
+  if (warp == 8) {
+    // ======================= TMA producer ===================================
+    if (lane == 0 && n_max > 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(&sm.q_full, 2 * C::TILE_BYTES);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_4d(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full, c * 64,
+                      rq0 + m0 + t * C::BM, h, bcoord);
+      int k_armed = 0, v_armed = 0;
+      for (int j = 0; j < n_max; ++j) {
+        const int s = j % C::NS;
+        const uint32_t ph = (j / C::NS) & 1;
+        if (!w.wait(&sm.k_empty[s], ph ^ 1, kErrPrefillKEmpty)) break;
+        mbar_arrive_expect_tx(&sm.k_full[s], C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_4d(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s], c * 64,
+                      rk0 + j * C::BN, hk, bcoord);
+        ++k_armed;
+        if (!w.wait(&sm.v_empty[s], ph ^ 1, kErrPrefillVEmpty)) break;
+        mbar_arrive_expect_tx(&sm.v_full[s], C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_4d(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s], c * 64,
+                      rk0 + j * C::BN, hk, bcoord);
+        ++v_armed;
+      }
+      if (w.aborted()) {
+        // Drain: every copy this CTA started must land before shared memory
+        // is released.  The last armed phase of each full barrier completes
+        // when its bytes arrive.
+        const uint64_t dl = globaltimer_ns() + 50000000ull;
+        wait_raw(&sm.q_full, 0, dl);
+        for (int jj = max(0, k_armed - C::NS); jj < k_armed; ++jj)
+          wait_raw(&sm.k_full[jj % C::NS], (jj / C::NS) & 1, dl);
+        for (int jj = max(0, v_armed - C::NS); jj < v_armed; ++jj)
+          wait_raw(&sm.v_full[jj % C::NS], (jj / C::NS) & 1, dl);
+      }
+    }
+  } else if (warp == 9) {
+    // ======================= MMA issuer (one thread) =========================
+    if (lane == 0 && n_max > 0) {
+      constexpr uint32_t idesc_s = idesc_f16_f32(BF16, 128, C::BN, false, false);
+      constexpr uint32_t idesc_o = idesc_f16_f32(BF16, 128, D, false, true);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t qa = smem_u32(sm.q[t]);
+        const uint32_t ka = smem_u32(sm.k[j % C::NS]);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
+          umma_ss(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024),
+                  sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&sm.s_full[t]);
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t va = smem_u32(sm.v[j % C::NS]);
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k) {
+          umma_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8,
+                  sdesc_sw128(va + k * 16 * 128, C::CHUNK_BYTES, 1024), idesc_o,
+                  (j > 0 || k > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = w.wait(&sm.q_full, 0, kErrPrefillQ);
+      if (ok) ok = w.wait(&sm.k_full[0], 0, kErrPrefillKFull);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (n_t[t] > 0) issue_s(t, 0);
+        umma_commit(&sm.k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int s = j % C::NS;
+        const uint32_t ph = (j / C::NS) & 1;
+        bool v_ready = false, kn_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= n_t[t]) continue;
+          if (!v_ready) {
+            ok = w.wait(&sm.v_full[s], ph, kErrPrefillVFull);
+            if (!ok) break;
+            v_ready = true;
+          }
+          ok = w.wait(&sm.p_full[t], j & 1, kErrPrefillPFull);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, j);
+          if (j + 1 < n_t[t]) {
+            if (!kn_ready) {
+              const int jn = j + 1;
+              ok = w.wait(&sm.k_full[jn % C::NS], (jn / C::NS) & 1, kErrPrefillKFull);
+              if (!ok) break;
+              tc_fence_after();
+              kn_ready = true;
+            }
+            issue_s(t, j + 1);
+          } else {
+            umma_commit(&sm.o_final[t]);
+          }
+        }
+        if (v_ready) umma_commit(&sm.v_empty[s]);
+        if (kn_ready) umma_commit(&sm.k_empty[(j + 1) % C::NS]);
+      }
+      // All MMAs this thread issued must finish before tensor memory is freed.
+      umma_commit(&sm.teardown);
+      if (!wait_raw(&sm.teardown, 0, globaltimer_ns() + 50000000ull) && p.err)
+        atomicOr(p.err, 1u << kErrPrefillTeardown);
+    }
+  } else {
+    // ======================= softmax warpgroups =============================
+    const int t = warp >> 2;           // query tile of this warpgroup
+    const int r = threadIdx.x & 127;   // row within the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + C::tm_s(t) + lane_base;
+    const uint32_t tO = tmem + C::tm_o(t) + lane_base;
+    const int mt = m0 + t * C::BM;
+    const int qi = mt + r;             // query index within the sequence
+    const int nt = n_t[t];
+    const int diag = Lk - Lq;          // bottom-right alignment offset
+
+    float m_use = -INFINITY;  // exp2 subtrahend currently in use (log2 units)
+    float l = 0.0f;           // running denominator w.r.t. m_use
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = __all_sync(0xffffffffu, w.wait(&sm.s_full[t], j & 1, kErrPrefillSFull));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[128];
+      {
+        uint32_t (&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+        uint32_t (&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+        uint32_t (&a2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
+        uint32_t (&a3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
+        tmem_ld32(tS + 0, a0);
+        tmem_ld32(tS + 32, a1);
+        tmem_ld32(tS + 64, a2);
+        tmem_ld32(tS + 96, a3);
+        tmem_ld_wait();
+        reg_fence(sr);
+      }
+      float x[128];
+      if constexpr (SOFTCAP) {
+        const float out_scale = p.softcap * kLog2e;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          x[c] = out_scale * tanh_via_exp2(__uint_as_float(sr[c]) * p.scale * p.softcap_inv);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]) * p.scale_log2;
+      }
+      const int j0 = j * C::BN;
+      const bool need_mask =
+          (j0 + C::BN > Lk) || (CAUSAL && (j0 + C::BN - 1 > mt + diag));
+      if (need_mask) {
+        int lim = Lk - 1 - j0;
+        if (CAUSAL) lim = min(lim, qi + diag - j0);
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      const float m_new = fmaxf(m_use, mx);
+      float alpha = 1.0f;
+      if (m_new - m_use > 8.0f) {  // false when both are -inf (NaN compare)
+        alpha = ex2_approx(m_use - m_new);
+        m_use = m_new;
+      }
+      const float msub = (m_use == -INFINITY) ? 0.0f : m_use;
+      float rs0 = 0.f, rs1 = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float p0 = ex2_approx(x[2 * i] - msub);
+        const float p1 = ex2_approx(x[2 * i + 1] - msub);
+        rs0 += p0;
+        rs1 += p1;
+        pk[i] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+      }
+      l = l * alpha + (rs0 + rs1);
+      tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      // The P.V MMA of the previous tile finished before this S was produced
+      // (its commit covers every earlier MMA), so O can be rescaled now.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c, ov);
+          tmem_ld_wait();
+          reg_fence(ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(tO + c, ov);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[t]);
+    }
+
+    // ---- epilogue: O = O / l, LSE = ln(l) + m (FA2 final rescale; FA3 store) --
+    const bool have_o = __all_sync(
+        0xffffffffu, ok && nt > 0 && w.wait(&sm.o_final[t], 0, kErrPrefillOFinal));
+    if (have_o) tc_fence_after();
+    const float msub = (m_use == -INFINITY) ? 0.0f : m_use;
+    float mfin = msub, ltot = l, oscale;
+    if (p.sink != nullptr) {
+      const float sl = p.sink[h] * kLog2e;
+      if (l > 0.0f) {
+        mfin = fmaxf(msub, sl);
+        const float a = ex2_approx(msub - mfin);
+        ltot = l * a + ex2_approx(sl - mfin);
+        oscale = a / ltot;
+      } else {
+        mfin = sl;
+        ltot = 1.0f;
+        oscale = 0.0f;
+      }
+    } else {
+      oscale = (l > 0.0f) ? 1.0f / l : 0.0f;
+    }
+    const bool row_ok = (qi < Lq) && (ok || nt == 0);
+    if (row_ok && p.lse != nullptr) {
+      const float lse = (ltot > 0.0f) ? (mfin + __log2f(ltot)) * kLn2 : -INFINITY;
+      p.lse[b * p.lse_batch + h * p.lse_head + rq0 + qi] = lse;
+    }
+    using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    T* orow = reinterpret_cast<T*>(p.o) + b * p.o_batch + h * p.o_head +
+              static_cast<int64_t>(rq0 + qi) * p.o_row;
+    if (have_o) {
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t ov[32];
+        tmem_ld32(tO + c, ov);
+        tmem_ld_wait();
+        reg_fence(ov);
+        if (row_ok) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = __uint_as_float(ov[2 * i]) * oscale;
+            const float bb = __uint_as_float(ov[2 * i + 1]) * oscale;
+            pk[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    } else if (row_ok) {
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL, bool SOFTCAP>
+static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream_t stream) {
+  using C = PrefillCfg<D>;
+  auto kern = attn_prefill_kernel<D, BF16, CAUSAL, SOFTCAP>;
+  const int smem = static_cast<int>(sizeof(PrefillSmem<C>)) + 1024;
+  static bool configured = false;  // per instantiation; attribute set is idempotent
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  kern<<<grid, C::THREADS, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool causal,
+                           bool softcap, cudaStream_t stream, char* name, size_t name_len) {
+  snprintf(name, name_len, "attn_prefill_tcgen05_d%d_%s_%s_%s_m256n128", d, bf16 ? "bf16" : "f16",
+           causal ? "causal" : "nomask", softcap ? "softcap" : "nocap");
+#define ATTN_PREFILL_CASE(D_, B_, C_, S_)                                        \
+  if (d == D_ && bf16 == B_ && causal == C_ && softcap == S_)                    \
+    return launch_prefill_t<D_, B_, C_, S_>(p, grid, stream);
+  ATTN_PREFILL_CASE(64, true, false, false)
+  ATTN_PREFILL_CASE(64, true, false, true)
+  ATTN_PREFILL_CASE(64, true, true, false)
+  ATTN_PREFILL_CASE(64, true, true, true)
+  ATTN_PREFILL_CASE(64, false, false, false)
+  ATTN_PREFILL_CASE(64, false, false, true)
+  ATTN_PREFILL_CASE(64, false, true, false)
+  ATTN_PREFILL_CASE(64, false, true, true)
+  ATTN_PREFILL_CASE(128, true, false, false)
+  ATTN_PREFILL_CASE(128, true, false, true)
+  ATTN_PREFILL_CASE(128, true, true, false)
+  ATTN_PREFILL_CASE(128, true, true, true)
+  ATTN_PREFILL_CASE(128, false, false, false)
+  ATTN_PREFILL_CASE(128, false, false, true)
+  ATTN_PREFILL_CASE(128, false, true, false)
+  ATTN_PREFILL_CASE(128, false, true, true)
+#undef ATTN_PREFILL_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn
