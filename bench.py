@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Benchmark of the fused attention forward on GB300.
+
+Default (one GPU): the dense causal prefill workload B4 H16 L2048 d128 bf16,
+metric = attention-forward TFLOP/s on unmasked (query, key) pairs.  The same
+run also measures the other full-size workloads (GQA long prefill, paged
+decode in GB/s, varlen softcap+sink prefill) and reports them under "extra".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then K steps; before every step a 256 MiB
+buffer is written so L2 (129 MB) holds nothing of the inputs; each step's
+kernels are bracketed by CUDA events recorded on the launching stream; the
+timed loop is bracketed by a barrier and a device synchronise.  nvidia-smi
+clocks are sampled during the timed loop.  Multi-GPU (torchrun): every rank
+runs its own independent batch (weak scaling, no data-path collective); the
+reported value is the sum of the work over the max time over ranks.
+--impl reference times the fp64 CPU oracle (the only reference this project
+has: the pages ship no runnable code) on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def kernel_source_sha(name: str) -> str:
+    path = os.path.join(ROOT, "attention_forward_13_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for f in (path, os.path.join(os.path.dirname(path), "ptx.cuh")):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload: str, source: str, scale_units: float = 1.0):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            d = json.load(fh)
+        e = d[workload]
+        if e.get("source_sha") != kernel_source_sha(source):
+            return None
+        return float(e["dram_bytes_per_launch"]) * scale_units
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# work accounting (algorithmic, from the definition; no kernel involvement)
+# ---------------------------------------------------------------------------
+def causal_pairs(Lq, Lk):
+    """Number of (i, j) with j <= i + (Lk - Lq), 0 <= j < Lk, 0 <= i < Lq."""
+    tot = 0
+    off = Lk - Lq
+    for i in range(Lq):
+        tot += max(0, min(Lk, i + off + 1))
+    return tot
+
+
+def dense_flops(B, Hq, Lq, Lk, d, causal):
+    pairs = causal_pairs(Lq, Lk) if causal else Lq * Lk
+    return 4.0 * d * B * Hq * pairs
+
+
+def varlen_flops(lens, Hq, d, causal):
+    return sum(4.0 * d * Hq * (causal_pairs(L, L) if causal else L * L) for L in lens)
+
+
+def paged_bytes(lens, Hkv, d, Lq, Hq, elem=2):
+    kv = sum(lens) * Hkv * d * elem * 2
+    qo = 2 * len(lens) * Lq * Hq * d * elem
+    return kv + qo + len(lens) * Hq * Lq * 4
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons during the timed loop."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(work_local: float, ms_local: float, world: int):
+    """Whole-job value: total work over all ranks / the slowest rank's time."""
+    if world == 1:
+        return work_local, ms_local
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([work_local, ms_local], dtype=torch.float64, device=dev)
+    w = t[:1].clone()
+    m = t[1:].clone()
+    dist.all_reduce(w, op=dist.ReduceOp.SUM)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX)
+    return float(w.item()), float(m.item())
+
+
+# ---------------------------------------------------------------------------
+def time_steps(fn, steps, warmup, stream, flush):
+    """W untimed steps, then K steps with a flush before each and events around fn."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def make_flush():
+    import torch
+    buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+
+    def flush():
+        buf.fill_(1.0)
+    return flush
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import attention_forward_13_gb300 as A
+    from attention_forward_13_gb300 import inputs
+
+    pk, pk_src = peaks()
+    stream = torch.cuda.current_stream()
+    flush = make_flush()
+    dev = "cuda"
+
+    # ---- headline: dense causal prefill B4 H16 L2048 d128 bf16 ---------------
+    B, H, L, d = 4, 16, 2048, 128
+    inp = inputs.dense(B, H, H, L, L, d, "bf16", seed=1002 + 1000 * rank, device=dev,
+                       causal=True)
+    o = torch.empty_like(inp.q)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    flops = dense_flops(B, H, L, L, d, True)
+
+    def step():
+        A.attn_fwd(inp.q, inp.k, inp.v, o=o, lse=lse, causal=True)
+
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    wall0 = time.perf_counter()
+    times = time_steps(step, args.steps, args.warmup, stream, flush)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    ms = statistics.mean(times)
+    total_flops, ms_max = aggregate(flops, ms, world)
+    tflops = total_flops / (ms_max * 1e-3) / 1e12
+    kern_tflops = flops / (ms * 1e-3) / 1e12
+
+    # ---- e2e through the public API with host buffers ------------------------
+    hq = inp.q.cpu().pin_memory()
+    hk = inp.k.cpu().pin_memory()
+    hv = inp.v.cpu().pin_memory()
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(inp.q), torch.empty_like(inp.k), torch.empty_like(inp.v)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        A.attn_fwd(dq, dk, dv, o=o, lse=lse, causal=True)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_times = time_steps(e2e_step, max(3, args.steps // 2), 2, stream, flush)
+    e2e_ms = statistics.mean(e2e_times)
+    e2e_flops, e2e_ms_max = aggregate(flops, e2e_ms, world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    result = {
+        "metric": "attn fwd TFLOPS (causal prefill, unmasked pairs) & % of GB300 bf16 tensor peak",
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16)",
+        "config": {"workload": "dense causal prefill B4 H16 L2048 d128 bf16 (bottom-right causal)",
+                   "B": B, "H": H, "seq_len": L, "head_dim": d, "causal": True,
+                   "parallelism": f"independent batch per GPU x{world}",
+                   "l2": "256 MiB buffer written before every step (flush)"},
+        "roofline": {"bound": "tensor", "achieved": round(kern_tflops, 2),
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(kern_tflops / pk["bf16_tflops"], 4),
+                     "traffic": traffic_for("prefill_B4H16L2048d128_causal", "prefill.cu"),
+                     "peak_source": f"{pk_src} bf16 burst (MEASURED_PEAKS.json)"
+                     if pk_src == "measured" else "fallback 1.9 PFLOP/s",
+                     "kernel": A.attn_last_kernel_name(),
+                     "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": round(e2e_flops / (e2e_ms_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms_max, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s_timed_loop": round(wall, 3),
+    }
+    if A.attn_device_error() != 0:
+        result["device_error"] = True
+
+    if not args.no_extra:
+        result["extra"] = run_extra(args, rank, pk, stream, flush)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return result
+
+
+def run_extra(args, rank, pk, stream, flush):
+    import torch
+    import attention_forward_13_gb300 as A
+    from attention_forward_13_gb300 import inputs
+
+    steps = max(3, args.steps // 2)
+    out = {}
+    # GQA long prefill
+    inp = inputs.workload(3, device="cuda")
+    fl = dense_flops(2, 32, 8192, 8192, 128, True)
+    t = time_steps(lambda: A.attn_fwd(inp.q, inp.k, inp.v, causal=True), steps, 3, stream, flush)
+    ms = statistics.mean(t)
+    out["gqa_causal_prefill_B2_Hq32_Hkv8_L8192_d128"] = {
+        "value": round(fl / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+        "roofline": {"bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}}
+    del inp
+    # paged decode
+    inp = inputs.workload(4, device="cuda")
+    bt, sl = inp.block_table.cuda(), inp.seqlens_k.cuda()
+    lens = inp.seqlens_k.tolist()
+    nb = paged_bytes(lens, 8, 128, 1, 32)
+    splits = A.attn_paged_auto_splits(64, 8, inp.block_table.shape[1])
+    ws = torch.empty(splits * 64 * 32 * 129, dtype=torch.float32, device="cuda")
+    o = torch.empty_like(inp.q)
+    lse = torch.empty((64, 32, 1), dtype=torch.float32, device="cuda")
+    t = time_steps(lambda: A.attn_fwd_paged(inp.q, inp.k_pool, inp.v_pool, bt, sl,
+                                            num_splits=splits, o=o, lse=lse, workspace=ws),
+                   steps, 3, stream, flush)
+    ms = statistics.mean(t)
+    gbs = nb / (ms * 1e-3) / 1e9
+    out["paged_decode_B64_Hq32_Hkv8_d128_page64"] = {
+        "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "splits": splits,
+        "algorithmic_bytes": nb,
+        "roofline": {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / pk["hbm_gbs"], 4)}}
+    del inp
+    # varlen softcap + sink
+    inp = inputs.workload(5, device="cuda")
+    cq, ck = inp.cu_seqlens_q.cuda(), inp.cu_seqlens_k.cuda()
+    lens = (inp.cu_seqlens_q[1:] - inp.cu_seqlens_q[:-1]).tolist()
+    fl = varlen_flops(lens, 16, 64, True)
+    t = time_steps(lambda: A.attn_fwd_varlen(inp.q, inp.k, inp.v, cq, ck, inp.max_seqlen_q,
+                                             causal=True, softcap=30.0, sink=inp.sink),
+                   steps, 3, stream, flush)
+    ms = statistics.mean(t)
+    out["varlen_causal_softcap_sink_16seq_H16_d64"] = {
+        "value": round(fl / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+        "roofline": {"bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}}
+    return out
+
+
+# ---------------------------------------------------------------------------
+def oracle_sample(n_heads):
+    """Inputs of n_heads (batch, head) problems of the headline workload:
+    1 x n_heads x 2048 x 128, causal (same shape as one slice of it)."""
+    from attention_forward_13_gb300 import inputs
+    inp = inputs.dense(1, n_heads, n_heads, 2048, 2048, 128, "bf16", seed=1002, causal=True)
+    import torch
+    return [t.to(torch.float64).numpy() for t in (inp.q, inp.k, inp.v)]
+
+
+def cpu_baseline(target_seconds=15.0):
+    """Time the fp64 oracle (as it stands) on a bounded sample of the headline
+    workload and report the same metric (TFLOP/s on unmasked pairs)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    q, k, v = oracle_sample(1)
+    t0 = time.perf_counter()
+    oracle.attn_dense(q, k, v, 1 / math.sqrt(128), True)
+    one = time.perf_counter() - t0  # wall of one head (single thread)
+    n = max(1, min(64, int(target_seconds * cores / max(one, 1e-3))))
+    q, k, v = oracle_sample(n)
+    t0 = time.perf_counter()
+    oracle.attn_dense(q, k, v, 1 / math.sqrt(128), True)
+    sec = time.perf_counter() - t0
+    fl = dense_flops(1, n, 2048, 2048, 128, True)
+    return {"value": round(fl / sec / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} of the 64 (batch, head) problems of the headline workload "
+                      f"(2048x2048 causal, d=128), fp64, {sec:.1f} s wall"}
+
+
+def run_reference(args, rank, world):
+    """The oracle timed as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return None
+    import oracle
+    cores = os.cpu_count() or 1
+    n = max(1, min(16, cores))
+    q, k, v = oracle_sample(n)
+    fl = dense_flops(1, n, 2048, 2048, 128, True)
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle.attn_dense(q[:, :1], k[:, :1], v[:, :1], 1 / math.sqrt(128), True)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.attn_dense(q, k, v, 1 / math.sqrt(128), True)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times)
+    val = fl / sec / 1e12
+    return {
+        "impl": "reference",
+        "metric": "attn fwd TFLOPS (causal prefill, unmasked pairs) & % of GB300 bf16 tensor peak",
+        "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "dense causal prefill B4 H16 L2048 d128 bf16 (bottom-right causal)",
+                   "sample": f"{n} (batch, head) problems per step"},
+        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{n} of 64 (batch, head) problems, fp64 oracle"},
+        "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.impl == "ours" and args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    rank, world, local = dist_setup(args)
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
