@@ -186,6 +186,33 @@ def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=No
     return o, lse_t
 
 
+def attn_fwd_paged_noalloc(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=None,
+                           lse=True, causal=False, scale=None, softcap=0.0, sink=None,
+                           stream=None):
+    """attn_fwd_paged for callers that cannot allocate device scratch: the split
+    partials live in a fixed 16 MiB array inside the library (shared by all
+    calls on a GPU; calls overlapping on the GPU race).  Outputs are allocated
+    here only when not given."""
+    B, Lq, Hq, d = q.shape
+    num_pages, page, Hkv, _ = k_pool.shape
+    if o is None:
+        o = torch.empty((B, Lq, Hq, d), dtype=q.dtype, device=q.device)
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+    sink = _check_sink(sink, Hq, q.device)
+    opts = _opts(scale, causal, softcap, sink)
+    st = library().attn_fwd_paged_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                          _ptr(seqlens_k), _ptr(o), _ptr(lse_t), B, Lq, Hq, Hkv,
+                                          d, _dtype_code(q), page, num_pages,
+                                          block_table.shape[1], num_splits, ctypes.byref(opts),
+                                          _stream(stream))
+    _check(st, "attn_fwd_paged_noalloc")
+    return o, lse_t
+
+
 def attn_splitkv_combine(o_partial, lse_partial, sink=None, dtype=torch.bfloat16, o=None,
                          lse=True, stream=None):
     """Merge split partials.  o_partial fp32 [S,B,Hq,Lq,d], lse_partial fp32 [S,B,Hq,Lq].

@@ -27,7 +27,9 @@ ATTN_F16, ATTN_BF16 = 0, 1
 
 EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_splitkv_combine",
            "attn_paged_workspace_bytes", "attn_paged_auto_splits", "attn_status_string",
-           "attn_last_kernel_name", "attn_device_error", "attn_selftest_timeout")
+           "attn_last_kernel_name", "attn_device_error", "attn_selftest_timeout",
+           "attn_fwd_paged_noalloc")
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -44,6 +46,8 @@ def _declare(lib):
                                     S, S, S, S, O, _P]
     lib.attn_fwd_paged.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                    _I, _I, _P, _P, O, _P]
+    lib.attn_fwd_paged_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                           _I, _I, _I, _I, O, _P]
     lib.attn_splitkv_combine.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]
     lib.attn_paged_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
     lib.attn_paged_workspace_bytes.restype = ctypes.c_size_t
@@ -56,7 +60,7 @@ def _declare(lib):
     lib.attn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.attn_selftest_timeout.argtypes = [ctypes.c_uint64, _P]
     for name in ("attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_splitkv_combine",
-                 "attn_device_error", "attn_selftest_timeout"):
+                 "attn_device_error", "attn_selftest_timeout", "attn_fwd_paged_noalloc"):
         getattr(lib, name).restype = _I
 
 

@@ -133,6 +133,34 @@ attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool
                            void* stream);
 
 /*
+ * attn_fwd_paged_noalloc -- attn_fwd_paged without caller-provided scratch.
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot allocate device memory when they call: a plugin inside a host
+ * engine that owns every allocation and gives plugins no allocator, a
+ * serving loop that must not call cudaMalloc (it can synchronise the device
+ * and take milliseconds), a runtime that reserved its memory budget up front.
+ *   Same arguments and results as attn_fwd_paged, minus o_partial and
+ *   lse_partial: the split scratch comes from a fixed array of
+ *   ATTN_NOALLOC_SCRATCH_BYTES inside this library, reserved on each GPU
+ *   that loads the library and held until the process exits.
+ *   An explicit num_splits whose scratch (attn_paged_workspace_bytes) would
+ *   exceed that size is rejected with ATTN_ERR_INVALID; num_splits = 0 picks
+ *   the automatic count, lowered until it fits.  The call allocates and
+ *   frees no device memory.  The first call on each device looks up the
+ *   array's address with that device current; make it before any stream
+ *   capture.  All calls on a device share the array: calls whose kernels
+ *   overlap on the GPU (unordered streams) race on it; calls ordered on one
+ *   stream are safe.  Nothing in the array needs to start at zero.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+attn_status attn_fwd_paged_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                                   const int32_t* block_table, const int32_t* seqlens_k, void* o,
+                                   float* lse, int B, int Lq, int Hq, int Hkv, int d,
+                                   attn_dtype dtype, int page_size, int num_pages,
+                                   int max_pages_per_seq, int num_splits, const attn_opts* opts,
+                                   void* stream);
+
+/*
  * attn_splitkv_combine -- LSE-weighted merge of split partials (derived from
  * the definition of LSE; FlashAttention-3 epilogue num_splits layout):
  *   M = max_s LSE_s,  w_s = exp(LSE_s - M),
