@@ -46,7 +46,14 @@ struct PrefillCfg {
   static constexpr int TILE_BYTES = BN * D * 2;  // one Q, K or V tile
   static constexpr int CHUNK_BYTES = BN * 128;   // one swizzle-atom column of a tile
   static constexpr int NS = (D == 128) ? 2 : 3;  // K/V ring depth
+#ifdef ATTN_PREFILL_WARPS10
   static constexpr int THREADS = 320;
+#else
+  // Three full warpgroups: the third (warps 8-11: TMA, MMA, two idle) gives
+  // registers to the two softmax warpgroups with setmaxnreg
+  // (3 warps x 168 regs per SMSP = 224 + 224 + 56).
+  static constexpr int THREADS = 384;
+#endif
   static constexpr uint32_t TM_COLS = 512;
   // Tensor-memory columns: S/P of tile t at 128*t, O of tile t at 256 + D*t.
   __device__ static constexpr uint32_t tm_s(int t) { return 128u * t; }
@@ -66,10 +73,92 @@ struct PrefillSmem {
   int abort_flag;
 };
 
-// tanh(y) = 1 - 2 / (exp(2y) + 1), with exp through the special-function unit.
-__device__ __forceinline__ float tanh_via_exp2(float y) {
-  const float e = ex2_approx(y * (2.0f * kLog2e));
-  return 1.0f - 2.0f * rcp_approx(e + 1.0f);
+// 2^x on the FMA pipe, for columns whose exponential is taken off the
+// special-function unit.  Cody-Waite style split x = j + f, j = round(x)
+// (adding and subtracting 1.5*2^23 rounds to an integer), f in [-1/2, 1/2];
+// 2^f from a degree-3 polynomial fitted for minimax relative error by the
+// Remez exchange on [-1/2, 1/2] (max relative error 7.5e-5, far below the
+// bf16/fp16 rounding P gets next); 2^j is added into the exponent field.
+// x is clamped to >= -126 so the exponent never wraps (-inf gives ~1e-38).
+__device__ __forceinline__ float exp2_poly3(float x) {
+  x = fmaxf(x, -126.0f);
+  const float t = x + 12582912.0f;
+  const float f = x - (t - 12582912.0f);
+  const float p = fmaf(fmaf(fmaf(0.05517166853f, f, 0.2426111251f), f, 0.6932609677f), f,
+                       0.9999280572f);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
+// Exponentials of the columns in each group of 8 whose index is below this
+// run on the FMA pipe (exp2_poly3); the rest use ex2.approx.
+#ifndef ATTN_POLY_PER8
+#define ATTN_POLY_PER8 0
+#endif
+constexpr int kPolyPer8 = ATTN_POLY_PER8;
+
+template <int C>
+__device__ __forceinline__ float exp2_mixed(float x) {
+  if constexpr ((C & 7) < kPolyPer8) return exp2_poly3(x);
+  else return ex2_approx(x);
+}
+
+// Maximum of 128 values: a tree of 3-input max instructions (64 instructions,
+// depth 5).
+__device__ __forceinline__ float max128(const float* v) {
+  float m[43];
+#pragma unroll
+  for (int i = 0; i < 42; ++i) m[i] = fmax3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  m[42] = fmaxf(v[126], v[127]);
+  float n[15];
+#pragma unroll
+  for (int i = 0; i < 14; ++i) n[i] = fmax3(m[3 * i], m[3 * i + 1], m[3 * i + 2]);
+  n[14] = m[42];
+  float o[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) o[i] = fmax3(n[3 * i], n[3 * i + 1], n[3 * i + 2]);
+  return fmaxf(fmax3(o[0], o[1], o[2]), fmaxf(o[3], o[4]));
+}
+
+// P for one row: p_c = 2^(s_c * a - b) for c < 128 (a = scale*log2e, or
+// cap*log2e when s holds tanh values), the FMA done two lanes at a time,
+// packed to bf16/fp16 pairs, with 4 packed partial sums (8 lanes).
+// MASK: columns past `lim` get p = 0 exactly (the polynomial path would give
+// ~1e-38 for -inf, and an all-masked row must keep l = 0); with every
+// exponential on ex2.approx, -inf already gives 0 and MASK adds nothing.
+template <bool BF16, bool MASK, int I = 0>
+__device__ __forceinline__ void exp_pack_row(const float* s, uint64_t a2, uint64_t nb2, int lim,
+                                             uint32_t* pk, uint64_t* acc2) {
+  if constexpr (I < 64) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(s[2 * I], s[2 * I + 1]), a2, nb2), x0, x1);
+    float p0 = exp2_mixed<2 * I>(x0);
+    float p1 = exp2_mixed<2 * I + 1>(x1);
+    if constexpr (MASK && kPolyPer8 > 0) {
+      p0 = (2 * I <= lim) ? p0 : 0.0f;
+      p1 = (2 * I + 1 <= lim) ? p1 : 0.0f;
+    }
+    acc2[I & 3] = f2_add(acc2[I & 3], f2_pack(p0, p1));
+    pk[I] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+    exp_pack_row<BF16, MASK, I + 1>(s, a2, nb2, lim, pk, acc2);
+  }
+}
+
+// tanh of 128 scaled scores in place: tanh(y) = 1 - 2 / (2^(2 y log2 e) + 1),
+// the multiplies, adds and FMA two lanes at a time.
+__device__ __forceinline__ void tanh128(float* s, float in_scale) {
+  const uint64_t k2 = f2_pack(in_scale * 2.0f * kLog2e, in_scale * 2.0f * kLog2e);
+  const uint64_t one2 = f2_pack(1.0f, 1.0f);
+  const uint64_t m2 = f2_pack(-2.0f, -2.0f);
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    float e0, e1;
+    f2_unpack(f2_mul(f2_pack(s[2 * i], s[2 * i + 1]), k2), e0, e1);
+    e0 = ex2_approx(e0);
+    e1 = ex2_approx(e1);
+    float d0, d1;
+    f2_unpack(f2_add(f2_pack(e0, e1), one2), d0, d1);
+    f2_unpack(f2_fma(f2_pack(rcp_approx(d0), rcp_approx(d1)), m2, one2), s[2 * i], s[2 * i + 1]);
+  }
 }
 
 // Wait for a barrier phase ignoring the abort flag (teardown only).
@@ -81,7 +170,7 @@ __device__ __forceinline__ bool wait_raw(uint64_t* bar, uint32_t parity, uint64_
 }
 
 template <int D, bool BF16, bool CAUSAL, bool SOFTCAP>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = PrefillCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -158,7 +247,10 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const Waiter w{globaltimer_ns() + p.timeout_ns, &sm.abort_flag, p.err};
-
+  if (warp >= 8) {
+#ifndef ATTN_PREFILL_WARPS10
+  setmaxnreg_dec<56>();
+#endif
   if (warp == 8) {
     // ======================= TMA producer ===================================
     if (lane == 0 && n_max > 0) {
@@ -272,7 +364,11 @@ __global__ void __launch_bounds__(320, 1)
       if (!wait_raw(&sm.teardown, 0, globaltimer_ns() + 50000000ull) && p.err)
         atomicOr(p.err, 1u << kErrPrefillTeardown);
     }
+  }  // warps 10, 11: no role
   } else {
+#ifndef ATTN_PREFILL_WARPS10
+    setmaxnreg_inc<224>();
+#endif
     // ======================= softmax warpgroups =============================
     const int t = warp >> 2;           // query tile of this warpgroup
     const int r = threadIdx.x & 127;   // row within the tile == TMEM lane
@@ -304,46 +400,42 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld_wait();
         reg_fence(sr);
       }
-      float x[128];
+      // Raw scores in place; the soft-cap variant turns them into capped
+      // log2-unit scores first, else the scale*log2(e) factor is folded into
+      // the exponent's FMA (CK MakeKargs FAST_EXP2 fold).
+      float* s = reinterpret_cast<float*>(sr);
+      float a_coef = p.scale_log2;
       if constexpr (SOFTCAP) {
-        const float out_scale = p.softcap * kLog2e;
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          x[c] = out_scale * tanh_via_exp2(__uint_as_float(sr[c]) * p.scale * p.softcap_inv);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]) * p.scale_log2;
+        tanh128(s, p.scale * p.softcap_inv);  // s <- tanh(scale * s / cap)
+        a_coef = p.softcap * kLog2e;          // capped score in log2 units = a_coef * s
       }
       const int j0 = j * C::BN;
       const bool need_mask =
           (j0 + C::BN > Lk) || (CAUSAL && (j0 + C::BN - 1 > mt + diag));
+      int lim = 127;
       if (need_mask) {
-        int lim = Lk - 1 - j0;
+        lim = Lk - 1 - j0;
         if (CAUSAL) lim = min(lim, qi + diag - j0);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
+        for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
       }
-      float mx = x[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
-      const float m_new = fmaxf(m_use, mx);
+      const float m_new = fmaxf(m_use, max128(s) * a_coef);  // a_coef > 0: order kept
       float alpha = 1.0f;
       if (m_new - m_use > 8.0f) {  // false when both are -inf (NaN compare)
         alpha = ex2_approx(m_use - m_new);
         m_use = m_new;
       }
       const float msub = (m_use == -INFINITY) ? 0.0f : m_use;
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pk[64];
+      uint64_t acc2[4];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2_approx(x[2 * i] - msub);
-        const float p1 = ex2_approx(x[2 * i + 1] - msub);
-        rs0 += p0;
-        rs1 += p1;
-        pk[i] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
-      }
-      l = l * alpha + (rs0 + rs1);
+      for (int i = 0; i < 4; ++i) acc2[i] = 0ull;  // +0.0f in both lanes
+      uint32_t pk[64];
+      const uint64_t a2 = f2_pack(a_coef, a_coef), nb2 = f2_pack(-msub, -msub);
+      if (need_mask) exp_pack_row<BF16, true>(s, a2, nb2, lim, pk, acc2);
+      else exp_pack_row<BF16, false>(s, a2, nb2, lim, pk, acc2);
+      float r0, r1;
+      f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), r0, r1);
+      l = l * alpha + (r0 + r1);
       tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       // The P.V MMA of the previous tile finished before this S was produced

@@ -320,57 +320,84 @@ def run_ours(args, rank, world, local):
     return result
 
 
-def run_extra(args, rank, pk, stream, flush):
+def run_extra(args, rank, pk, stream, flush, only=None):
     import torch
     import attention_forward_13_gb300 as A
     from attention_forward_13_gb300 import inputs
 
-    steps = max(3, args.steps // 2)
+    steps = max(3, args.steps // 2) if only is None else args.steps
+    warm = 3 if only is None else args.warmup
     out = {}
-    # GQA long prefill
+    if only in (None, "gqa"):
+        out.update(_extra_gqa(A, inputs, pk, stream, flush, steps, warm))
+    if only in (None, "decode"):
+        out.update(_extra_decode(A, inputs, pk, stream, flush, steps, warm, args.decode_batch))
+    if only in (None, "varlen"):
+        out.update(_extra_varlen(A, inputs, pk, stream, flush, steps, warm))
+    return out
+
+
+def _extra_gqa(A, inputs, pk, stream, flush, steps, warm):
     inp = inputs.workload(3, device="cuda")
     fl = dense_flops(2, 32, 8192, 8192, 128, True)
-    t = time_steps(lambda: A.attn_fwd(inp.q, inp.k, inp.v, causal=True), steps, 3, stream, flush)
+    t = time_steps(lambda: A.attn_fwd(inp.q, inp.k, inp.v, causal=True), steps, warm, stream,
+                   flush)
     ms = statistics.mean(t)
-    out["gqa_causal_prefill_B2_Hq32_Hkv8_L8192_d128"] = {
+    return {"gqa_causal_prefill_B2_Hq32_Hkv8_L8192_d128": {
         "value": round(fl / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+        "kernel": A.attn_last_kernel_name(),
         "roofline": {"bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}}
-    del inp
-    # paged decode
-    inp = inputs.workload(4, device="cuda")
-    bt, sl = inp.block_table.cuda(), inp.seqlens_k.cuda()
-    lens = inp.seqlens_k.tolist()
+                     "frac": round(fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}}}
+
+
+def _extra_decode(A, inputs, pk, stream, flush, steps, warm, batch):
+    """Paged decode workload; batch < 64 keeps the first `batch` sequence
+    lengths of the workload with a pool of just the pages they need (a smaller
+    case for profiling: a few hundred MB on the device)."""
+    import torch
+    B = min(64, batch)
+    if B == 64:
+        inp = inputs.workload(4, device="cuda")
+    else:
+        lens_all = inputs.random_lengths(64, 512, 8192, seed=1004)[:B]
+        npg = sum((L + 63) // 64 for L in lens_all)
+        inp = inputs.paged(lens_all, 1, 32, 8, 128, 64, npg + 16, max_pages=128, seed=1004,
+                           device="cuda")
+    q = inp.q[:B].contiguous()
+    bt, sl = inp.block_table[:B].cuda(), inp.seqlens_k[:B].cuda()
+    lens = inp.seqlens_k[:B].tolist()
     nb = paged_bytes(lens, 8, 128, 1, 32)
-    splits = A.attn_paged_auto_splits(64, 8, inp.block_table.shape[1])
-    ws = torch.empty(splits * 64 * 32 * 129, dtype=torch.float32, device="cuda")
-    o = torch.empty_like(inp.q)
-    lse = torch.empty((64, 32, 1), dtype=torch.float32, device="cuda")
-    t = time_steps(lambda: A.attn_fwd_paged(inp.q, inp.k_pool, inp.v_pool, bt, sl,
+    splits = A.attn_paged_auto_splits(B, 8, inp.block_table.shape[1])
+    ws = torch.empty(max(1, splits * B * 32 * 129), dtype=torch.float32, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, 32, 1), dtype=torch.float32, device="cuda")
+    t = time_steps(lambda: A.attn_fwd_paged(q, inp.k_pool, inp.v_pool, bt, sl,
                                             num_splits=splits, o=o, lse=lse, workspace=ws),
-                   steps, 3, stream, flush)
+                   steps, warm, stream, flush)
     ms = statistics.mean(t)
     gbs = nb / (ms * 1e-3) / 1e9
-    out["paged_decode_B64_Hq32_Hkv8_d128_page64"] = {
+    key = "paged_decode_B64_Hq32_Hkv8_d128_page64" if B == 64 else f"paged_decode_B{B}_Hq32_Hkv8_d128_page64"
+    return {key: {
         "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "splits": splits,
-        "algorithmic_bytes": nb,
+        "algorithmic_bytes": nb, "kernel": A.attn_last_kernel_name(),
         "roofline": {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(gbs / pk["hbm_gbs"], 4)}}
-    del inp
-    # varlen softcap + sink
+                     "frac": round(gbs / pk["hbm_gbs"], 4)}}}
+
+
+def _extra_varlen(A, inputs, pk, stream, flush, steps, warm):
     inp = inputs.workload(5, device="cuda")
     cq, ck = inp.cu_seqlens_q.cuda(), inp.cu_seqlens_k.cuda()
     lens = (inp.cu_seqlens_q[1:] - inp.cu_seqlens_q[:-1]).tolist()
     fl = varlen_flops(lens, 16, 64, True)
     t = time_steps(lambda: A.attn_fwd_varlen(inp.q, inp.k, inp.v, cq, ck, inp.max_seqlen_q,
                                              causal=True, softcap=30.0, sink=inp.sink),
-                   steps, 3, stream, flush)
+                   steps, warm, stream, flush)
     ms = statistics.mean(t)
-    out["varlen_causal_softcap_sink_16seq_H16_d64"] = {
+    return {"varlen_causal_softcap_sink_16seq_H16_d64": {
         "value": round(fl / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+        "kernel": A.attn_last_kernel_name(),
         "roofline": {"bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}}
-    return out
+                     "frac": round(fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}}}
 
 
 # ---------------------------------------------------------------------------
@@ -449,6 +476,9 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--only", choices=["gqa", "decode", "varlen"], default=None,
+                    help="run one secondary workload alone (profiling) and print its line")
+    ap.add_argument("--decode-batch", type=int, default=64)
     args = ap.parse_args()
     if args.impl == "ours" and args.warmup < 3:
         args.warmup = 3
@@ -460,6 +490,15 @@ def main():
             print(json.dumps(res))
         return
     rank, world, local = dist_setup(args)
+    if args.only is not None:
+        import torch
+        pk, _ = peaks()
+        res = {"only": args.only, "steps": args.steps, "warmup": args.warmup,
+               "results": run_extra(args, rank, pk, torch.cuda.current_stream(), make_flush(),
+                                    only=args.only)}
+        if rank == 0:
+            print(json.dumps(res))
+        return
     res = run_ours(args, rank, world, local)
     if rank == 0:
         print(json.dumps(res))
