@@ -217,7 +217,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   PrefillParams p;
   memset(&p, 0, sizeof(p));
   unsigned int* err = nullptr;
-  if (device_state(&err, nullptr) != ATTN_OK) return ATTN_ERR_CUDA;
+  int num_sms = 0;
+  if (device_state(&err, &num_sms) != ATTN_OK) return ATTN_ERR_CUDA;
   const bool bf16 = dtype == ATTN_BF16;
   const uint32_t box[4] = {64, 128, 1, 1};
   {
@@ -256,7 +257,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.err = err;
   fill_common(p, opts, d);
   const bool causal = opts != nullptr && opts->causal != 0;
-  const int grid = p.num_m_blocks * B * Hq;
+  p.num_items = p.num_m_blocks * B * Hq;
+  const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
   return finish_launch(launch_prefill(p, grid, d, bf16, causal, p.softcap > 0.0f,
                                       static_cast<cudaStream_t>(stream), g_last_name,
                                       sizeof(g_last_name)));
@@ -287,7 +289,8 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   PrefillParams p;
   memset(&p, 0, sizeof(p));
   unsigned int* err = nullptr;
-  if (device_state(&err, nullptr) != ATTN_OK) return ATTN_ERR_CUDA;
+  int num_sms = 0;
+  if (device_state(&err, &num_sms) != ATTN_OK) return ATTN_ERR_CUDA;
   const bool bf16 = dtype == ATTN_BF16;
   const uint32_t box[4] = {64, 128, 1, 1};
   {
@@ -331,7 +334,8 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   p.err = err;
   fill_common(p, opts, d);
   const bool causal = opts != nullptr && opts->causal != 0;
-  const int grid = p.num_m_blocks * B * Hq;
+  p.num_items = p.num_m_blocks * B * Hq;
+  const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
   return finish_launch(launch_prefill(p, grid, d, bf16, causal, p.softcap > 0.0f,
                                       static_cast<cudaStream_t>(stream), g_last_name,
                                       sizeof(g_last_name)));
@@ -348,9 +352,14 @@ int attn_paged_auto_splits(int B, int Hkv, int max_pages_per_seq) {
   device_state(nullptr, &sms);
   if (B <= 0 || Hkv <= 0 || max_pages_per_seq <= 0) return 1;
   // Aim for about two resident CTAs per SM worth of (sequence, kv head, split)
-  // work items, but never fewer than ~8 pages (512 keys at page 64) per split.
+  // work items and at most 32 pages per split (the longest CTA bounds the
+  // tail), but never fewer than ~8 pages (512 keys at page 64) per split:
+  // every CTA pays a fixed start-up cost (measured on the decode workload:
+  // 4 splits best, 12 or more clearly worse).
   const int64_t pairs = static_cast<int64_t>(B) * Hkv;
   int64_t want = (4LL * sms + pairs - 1) / pairs;
+  const int64_t by_len = (max_pages_per_seq + 31) / 32;
+  if (want < by_len) want = by_len;
   const int64_t max_useful = (max_pages_per_seq + 7) / 8;
   if (want > max_useful) want = max_useful;
   if (want < 1) want = 1;

@@ -46,6 +46,7 @@ struct PrefillParams {
   int B, Hq, Hkv, Lq, Lk;          // batch-mode lengths (ignored for varlen)
   int total_q, total_k;            // varlen: packed extents (sequences are clamped to them)
   int num_m_blocks;                // 256-row query blocks per (b, h)
+  int num_items;                   // num_m_blocks * B * Hq work items
   float scale_log2;                // scale * log2(e)
   float scale;                     // plain scale (soft-cap path)
   float softcap;                   // cap (> 0 when the soft-cap variant runs)

@@ -12,11 +12,14 @@
 // GQA kv head = h / ratio, heaviest causal tiles first, the scale*log2(e)
 // fold).  The Blackwell design here differs from all three:
 //
-//  * one CTA owns TWO 128-row query tiles of one (batch, head) and streams
-//    128-key K/V tiles once for both; warps 0-3 run the softmax of tile 0,
-//    warps 4-7 that of tile 1, warp 8 issues TMA, warp 9 issues tcgen05.mma.
-//    While one warpgroup computes exponentials the tensor core works on the
-//    other tile (ping-pong).
+//  * persistent: one CTA per SM walks a list of work items (a 256-row query
+//    block of one (batch, head)), heaviest causal blocks first, in snake
+//    order across CTAs.  The next item's Q load and its first S = Q K^T
+//    overlap the current item's last P.V and epilogue.
+//  * each item is two 128-row query tiles sharing every 128-key K/V tile;
+//    warps 0-3 run the softmax of tile 0, warps 4-7 that of tile 1, warp 8
+//    issues TMA, warp 9 issues tcgen05.mma.  While one warpgroup computes
+//    exponentials the tensor core works on the other tile (ping-pong).
 //  * S lives in tensor memory (fp32, 128 columns per tile).  The softmax
 //    writes P (bf16/fp16) back over the first 64 columns of its S and the
 //    P.V MMA reads its A operand straight from tensor memory.
@@ -46,14 +49,10 @@ struct PrefillCfg {
   static constexpr int TILE_BYTES = BN * D * 2;  // one Q, K or V tile
   static constexpr int CHUNK_BYTES = BN * 128;   // one swizzle-atom column of a tile
   static constexpr int NS = (D == 128) ? 2 : 3;  // K/V ring depth
-#ifdef ATTN_PREFILL_WARPS10
-  static constexpr int THREADS = 320;
-#else
   // Three full warpgroups: the third (warps 8-11: TMA, MMA, two idle) gives
   // registers to the two softmax warpgroups with setmaxnreg
-  // (3 warps x 168 regs per SMSP = 224 + 224 + 56).
+  // (launch: 384 x 168 = 64512 registers; after: 256 x 200 + 128 x 96 = 63488).
   static constexpr int THREADS = 384;
-#endif
   static constexpr uint32_t TM_COLS = 512;
   // Tensor-memory columns: S/P of tile t at 128*t, O of tile t at 256 + D*t.
   __device__ static constexpr uint32_t tm_s(int t) { return 128u * t; }
@@ -65,42 +64,13 @@ struct PrefillSmem {
   alignas(1024) uint8_t q[2][C::TILE_BYTES];
   alignas(1024) uint8_t k[C::NS][C::TILE_BYTES];
   alignas(1024) uint8_t v[C::NS][C::TILE_BYTES];
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t k_full[C::NS], k_empty[C::NS], v_full[C::NS], v_empty[C::NS];
-  uint64_t s_full[2], p_full[2], o_final[2];
+  uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
   uint64_t teardown;
   uint32_t tmem_base;
   int abort_flag;
 };
-
-// 2^x on the FMA pipe, for columns whose exponential is taken off the
-// special-function unit.  Cody-Waite style split x = j + f, j = round(x)
-// (adding and subtracting 1.5*2^23 rounds to an integer), f in [-1/2, 1/2];
-// 2^f from a degree-3 polynomial fitted for minimax relative error by the
-// Remez exchange on [-1/2, 1/2] (max relative error 7.5e-5, far below the
-// bf16/fp16 rounding P gets next); 2^j is added into the exponent field.
-// x is clamped to >= -126 so the exponent never wraps (-inf gives ~1e-38).
-__device__ __forceinline__ float exp2_poly3(float x) {
-  x = fmaxf(x, -126.0f);
-  const float t = x + 12582912.0f;
-  const float f = x - (t - 12582912.0f);
-  const float p = fmaf(fmaf(fmaf(0.05517166853f, f, 0.2426111251f), f, 0.6932609677f), f,
-                       0.9999280572f);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
-// Exponentials of the columns in each group of 8 whose index is below this
-// run on the FMA pipe (exp2_poly3); the rest use ex2.approx.
-#ifndef ATTN_POLY_PER8
-#define ATTN_POLY_PER8 0
-#endif
-constexpr int kPolyPer8 = ATTN_POLY_PER8;
-
-template <int C>
-__device__ __forceinline__ float exp2_mixed(float x) {
-  if constexpr ((C & 7) < kPolyPer8) return exp2_poly3(x);
-  else return ex2_approx(x);
-}
 
 // Maximum of 128 values: a tree of 3-input max instructions (64 instructions,
 // depth 5).
@@ -121,25 +91,19 @@ __device__ __forceinline__ float max128(const float* v) {
 
 // P for one row: p_c = 2^(s_c * a - b) for c < 128 (a = scale*log2e, or
 // cap*log2e when s holds tanh values), the FMA done two lanes at a time,
-// packed to bf16/fp16 pairs, with 4 packed partial sums (8 lanes).
-// MASK: columns past `lim` get p = 0 exactly (the polynomial path would give
-// ~1e-38 for -inf, and an all-masked row must keep l = 0); with every
-// exponential on ex2.approx, -inf already gives 0 and MASK adds nothing.
-template <bool BF16, bool MASK, int I = 0>
-__device__ __forceinline__ void exp_pack_row(const float* s, uint64_t a2, uint64_t nb2, int lim,
+// packed to bf16/fp16 pairs, with 4 packed partial sums (8 lanes).  A masked
+// score is -inf and gives p = 0 exactly.
+template <bool BF16, int I = 0>
+__device__ __forceinline__ void exp_pack_row(const float* s, uint64_t a2, uint64_t nb2,
                                              uint32_t* pk, uint64_t* acc2) {
   if constexpr (I < 64) {
     float x0, x1;
     f2_unpack(f2_fma(f2_pack(s[2 * I], s[2 * I + 1]), a2, nb2), x0, x1);
-    float p0 = exp2_mixed<2 * I>(x0);
-    float p1 = exp2_mixed<2 * I + 1>(x1);
-    if constexpr (MASK && kPolyPer8 > 0) {
-      p0 = (2 * I <= lim) ? p0 : 0.0f;
-      p1 = (2 * I + 1 <= lim) ? p1 : 0.0f;
-    }
+    const float p0 = ex2_approx(x0);
+    const float p1 = ex2_approx(x1);
     acc2[I & 3] = f2_add(acc2[I & 3], f2_pack(p0, p1));
     pk[I] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
-    exp_pack_row<BF16, MASK, I + 1>(s, a2, nb2, lim, pk, acc2);
+    exp_pack_row<BF16, I + 1>(s, a2, nb2, pk, acc2);
   }
 }
 
@@ -169,6 +133,67 @@ __device__ __forceinline__ bool wait_raw(uint64_t* bar, uint32_t parity, uint64_
   return true;
 }
 
+// One unit of work: a 256-row query block (two 128-row tiles) of one
+// (batch, query head) against all of its keys.
+struct PrefillItem {
+  int b, h, hk, rq0, rk0, bcoord, Lq, Lk, m0;
+  int n[2];  // K/V tiles needed by query tile 0 / 1 (0: no key, or no row)
+  int nmax;
+};
+
+// Item index -> coordinates.  Causal problems list the heaviest query blocks
+// first (Composable Kernel GetTileIndex reverses the m-tile order when
+// masking).  Returns false when the block starts past the sequence end.
+template <int BM, int BN, bool CAUSAL>
+__device__ __forceinline__ bool decode_item(const PrefillParams& p, int item, PrefillItem& it) {
+  const int nbh = p.B * p.Hq;
+  const int mb_i = item / nbh;
+  const int bh = item - mb_i * nbh;
+  const int mb = CAUSAL ? (p.num_m_blocks - 1 - mb_i) : mb_i;
+  it.h = bh % p.Hq;
+  it.b = bh / p.Hq;
+  it.hk = it.h / (p.Hq / p.Hkv);
+  it.Lq = p.Lq;
+  it.Lk = p.Lk;
+  it.rq0 = 0;
+  it.rk0 = 0;
+  it.bcoord = it.b;
+  if (p.cu_q != nullptr) {  // group mode (Composable Kernel seqstart_q/k)
+    it.rq0 = p.cu_q[it.b];
+    it.Lq = p.cu_q[it.b + 1] - it.rq0;
+    it.rk0 = p.cu_k[it.b];
+    it.Lk = p.cu_k[it.b + 1] - it.rk0;
+    it.bcoord = 0;
+    // Sequences never reach past the packed tensors, whatever cu_seqlens holds.
+    if (it.rq0 < 0 || it.rq0 > p.total_q) it.Lq = 0;
+    it.Lq = min(it.Lq, p.total_q - it.rq0);
+    if (it.rk0 < 0 || it.rk0 > p.total_k) it.Lk = 0;
+    it.Lk = max(0, min(it.Lk, p.total_k - it.rk0));
+  }
+  it.m0 = mb * 2 * BM;
+  if (it.m0 >= it.Lq) return false;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int mt = it.m0 + t * BM;
+    if (mt >= it.Lq) {
+      it.n[t] = 0;
+    } else {
+      const int last = min(mt + BM - 1, it.Lq - 1);
+      const int kend = CAUSAL ? min(it.Lk, last + (it.Lk - it.Lq) + 1) : it.Lk;
+      it.n[t] = kend > 0 ? (kend + BN - 1) / BN : 0;
+    }
+  }
+  it.nmax = max(it.n[0], it.n[1]);
+  return true;
+}
+
+// The r-th item of this CTA: rounds of gridDim.x items, alternating direction
+// (snake), so the heavy head of the list is spread evenly across CTAs.
+__device__ __forceinline__ int item_of_round(int r) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
 template <int D, bool BF16, bool CAUSAL, bool SOFTCAP>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ PrefillParams p) {
@@ -177,52 +202,12 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   PrefillSmem<C>& sm = *reinterpret_cast<PrefillSmem<C>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  // ---- which (query block, head, batch) this CTA owns -----------------------
-  // Causal problems run the heaviest query blocks first (Composable Kernel
-  // GetTileIndex reverses the m-tile order when masking).
-  const int nbh = p.B * p.Hq;
-  const int mb_i = blockIdx.x / nbh;
-  const int bh = blockIdx.x - mb_i * nbh;
-  const int mb = CAUSAL ? (p.num_m_blocks - 1 - mb_i) : mb_i;
-  const int h = bh % p.Hq;
-  const int b = bh / p.Hq;
-  const int hk = h / (p.Hq / p.Hkv);
-  int Lq = p.Lq, Lk = p.Lk, rq0 = 0, rk0 = 0, bcoord = b;
-  if (p.cu_q != nullptr) {  // group mode (Composable Kernel seqstart_q/k)
-    rq0 = p.cu_q[b];
-    Lq = p.cu_q[b + 1] - rq0;
-    rk0 = p.cu_k[b];
-    Lk = p.cu_k[b + 1] - rk0;
-    bcoord = 0;
-    // Sequences never reach past the packed tensors, whatever cu_seqlens holds.
-    if (rq0 < 0 || rq0 > p.total_q) Lq = 0;
-    Lq = min(Lq, p.total_q - rq0);
-    if (rk0 < 0 || rk0 > p.total_k) Lk = 0;
-    Lk = max(0, min(Lk, p.total_k - rk0));
-  }
-  const int m0 = mb * 2 * C::BM;
-  if (m0 >= Lq) return;  // uniform early exit, nothing set up yet
-
-  // KV tiles each query tile needs.
-  int n_t[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int mt = m0 + t * C::BM;
-    if (mt >= Lq) {
-      n_t[t] = 0;
-    } else {
-      const int last = min(mt + C::BM - 1, Lq - 1);
-      const int kend = CAUSAL ? min(Lk, last + (Lk - Lq) + 1) : Lk;
-      n_t[t] = kend > 0 ? (kend + C::BN - 1) / C::BN : 0;
-    }
-  }
-  const int n_max = max(n_t[0], n_t[1]);
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
@@ -233,6 +218,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       mbar_init(&sm.s_full[t], 1);
       mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_final[t], 1);
+      mbar_init(&sm.o_free[t], 128);
     }
     mbar_init(&sm.teardown, 1);
     sm.abort_flag = 0;
@@ -247,62 +233,68 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const Waiter w{globaltimer_ns() + p.timeout_ns, &sm.abort_flag, p.err};
+
   if (warp >= 8) {
-#ifndef ATTN_PREFILL_WARPS10
-  setmaxnreg_dec<56>();
-#endif
-  if (warp == 8) {
-    // ======================= TMA producer ===================================
-    if (lane == 0 && n_max > 0) {
+    setmaxnreg_dec<96>();
+    if (warp == 8 && lane == 0) {
+      // ===================== TMA producer =====================================
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(&sm.q_full, 2 * C::TILE_BYTES);
+      int g = 0, qn = 0, k_armed = 0, v_armed = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int item = item_of_round(r);
+        if (item >= p.num_items) break;
+        PrefillItem it;
+        if (!decode_item<C::BM, C::BN, CAUSAL>(p, item, it) || it.nmax == 0) continue;
+        // The previous item's S MMAs must be done with the Q buffer.
+        if (qn > 0 && !(ok = w.wait(&sm.q_empty, (qn - 1) & 1, kErrPrefillQ))) break;
+        mbar_arrive_expect_tx(&sm.q_full, 2 * C::TILE_BYTES);
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_4d(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full, c * 64,
-                      rq0 + m0 + t * C::BM, h, bcoord);
-      int k_armed = 0, v_armed = 0;
-      for (int j = 0; j < n_max; ++j) {
-        const int s = j % C::NS;
-        const uint32_t ph = (j / C::NS) & 1;
-        if (!w.wait(&sm.k_empty[s], ph ^ 1, kErrPrefillKEmpty)) break;
-        mbar_arrive_expect_tx(&sm.k_full[s], C::TILE_BYTES);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_4d(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full, c * 64,
+                        it.rq0 + it.m0 + t * C::BM, it.h, it.bcoord);
+        ++qn;
+        for (int j = 0; j < it.nmax; ++j, ++g) {
+          const int s = g % C::NS;
+          const uint32_t ph = (g / C::NS) & 1;
+          if (!(ok = w.wait(&sm.k_empty[s], ph ^ 1, kErrPrefillKEmpty))) break;
+          mbar_arrive_expect_tx(&sm.k_full[s], C::TILE_BYTES);
 #pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_4d(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s], c * 64,
-                      rk0 + j * C::BN, hk, bcoord);
-        ++k_armed;
-        if (!w.wait(&sm.v_empty[s], ph ^ 1, kErrPrefillVEmpty)) break;
-        mbar_arrive_expect_tx(&sm.v_full[s], C::TILE_BYTES);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_4d(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s], c * 64,
+                        it.rk0 + j * C::BN, it.hk, it.bcoord);
+          ++k_armed;
+          if (!(ok = w.wait(&sm.v_empty[s], ph ^ 1, kErrPrefillVEmpty))) break;
+          mbar_arrive_expect_tx(&sm.v_full[s], C::TILE_BYTES);
 #pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_4d(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s], c * 64,
-                      rk0 + j * C::BN, hk, bcoord);
-        ++v_armed;
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_4d(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s], c * 64,
+                        it.rk0 + j * C::BN, it.hk, it.bcoord);
+          ++v_armed;
+        }
       }
       if (w.aborted()) {
         // Drain: every copy this CTA started must land before shared memory
         // is released.  The last armed phase of each full barrier completes
         // when its bytes arrive.
         const uint64_t dl = globaltimer_ns() + 50000000ull;
-        wait_raw(&sm.q_full, 0, dl);
+        if (qn > 0) wait_raw(&sm.q_full, (qn - 1) & 1, dl);
         for (int jj = max(0, k_armed - C::NS); jj < k_armed; ++jj)
           wait_raw(&sm.k_full[jj % C::NS], (jj / C::NS) & 1, dl);
         for (int jj = max(0, v_armed - C::NS); jj < v_armed; ++jj)
           wait_raw(&sm.v_full[jj % C::NS], (jj / C::NS) & 1, dl);
       }
-    }
-  } else if (warp == 9) {
-    // ======================= MMA issuer (one thread) =========================
-    if (lane == 0 && n_max > 0) {
+    } else if (warp == 9 && lane == 0) {
+      // ===================== MMA issuer (one thread) ===========================
       constexpr uint32_t idesc_s = idesc_f16_f32(BF16, 128, C::BN, false, false);
       constexpr uint32_t idesc_o = idesc_f16_f32(BF16, 128, D, false, true);
-      auto issue_s = [&](int t, int j) {
+      auto issue_s = [&](int t, int g) {  // S_t = Q_t K_g^T
         const uint32_t qa = smem_u32(sm.q[t]);
-        const uint32_t ka = smem_u32(sm.k[j % C::NS]);
+        const uint32_t ka = smem_u32(sm.k[g % C::NS]);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
@@ -311,206 +303,239 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         }
         umma_commit(&sm.s_full[t]);
       };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t va = smem_u32(sm.v[j % C::NS]);
+      auto issue_pv = [&](int t, int g, bool acc) {  // O_t (+)= P_t V_g
+        const uint32_t va = smem_u32(sm.v[g % C::NS]);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {
           umma_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8,
                   sdesc_sw128(va + k * 16 * 128, C::CHUNK_BYTES, 1024), idesc_o,
-                  (j > 0 || k > 0) ? 1u : 0u);
+                  (acc || k > 0) ? 1u : 0u);
         }
       };
-      bool ok = w.wait(&sm.q_full, 0, kErrPrefillQ);
-      if (ok) ok = w.wait(&sm.k_full[0], 0, kErrPrefillKFull);
-      if (ok) {
+      int g = 0, qn = 0;
+      int pc[2] = {0, 0};  // participations of each tile so far (p_full phases)
+      int oc[2] = {0, 0};  // items finished by each tile so far (o_free phases)
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int item = item_of_round(r);
+        if (item >= p.num_items) break;
+        PrefillItem it;
+        if (!decode_item<C::BM, C::BN, CAUSAL>(p, item, it) || it.nmax == 0) continue;
+        ok = w.wait(&sm.q_full, qn & 1, kErrPrefillQ) &&
+             w.wait(&sm.k_full[g % C::NS], (g / C::NS) & 1, kErrPrefillKFull);
+        ++qn;
+        if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (n_t[t] > 0) issue_s(t, 0);
-        umma_commit(&sm.k_empty[0]);
-      }
-      for (int j = 0; ok && j < n_max; ++j) {
-        const int s = j % C::NS;
-        const uint32_t ph = (j / C::NS) & 1;
-        bool v_ready = false, kn_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= n_t[t]) continue;
-          if (!v_ready) {
-            ok = w.wait(&sm.v_full[s], ph, kErrPrefillVFull);
-            if (!ok) break;
-            v_ready = true;
-          }
-          ok = w.wait(&sm.p_full[t], j & 1, kErrPrefillPFull);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, j);
-          if (j + 1 < n_t[t]) {
-            if (!kn_ready) {
-              const int jn = j + 1;
-              ok = w.wait(&sm.k_full[jn % C::NS], (jn / C::NS) & 1, kErrPrefillKFull);
-              if (!ok) break;
-              tc_fence_after();
-              kn_ready = true;
+          if (it.n[t] > 0) issue_s(t, g);
+        umma_commit(&sm.k_empty[g % C::NS]);
+        // Q is free for the next item once the item's last S MMA completes:
+        // commit right after that issue so the next Q load overlaps the tail.
+        if (it.nmax == 1) umma_commit(&sm.q_empty);
+        for (int j = 0; ok && j < it.nmax; ++j) {
+          const int gj = g + j;
+          const int s = gj % C::NS;
+          bool v_ready = false, kn_ready = false;
+          for (int t = 0; t < 2; ++t) {
+            if (j >= it.n[t]) continue;
+            if (!v_ready) {
+              if (!(ok = w.wait(&sm.v_full[s], (gj / C::NS) & 1, kErrPrefillVFull))) break;
+              v_ready = true;
             }
-            issue_s(t, j + 1);
-          } else {
-            umma_commit(&sm.o_final[t]);
+            if (!(ok = w.wait(&sm.p_full[t], pc[t] & 1, kErrPrefillPFull))) break;
+            ++pc[t];
+            // O_t is free once the previous item's epilogue has read it.
+            if (j == 0 && oc[t] > 0 &&
+                !(ok = w.wait(&sm.o_free[t], (oc[t] - 1) & 1, kErrPrefillOFinal)))
+              break;
+            tc_fence_after();
+            issue_pv(t, gj, j > 0);
+            if (j + 1 < it.n[t]) {
+              if (!kn_ready) {
+                const int gn = gj + 1;
+                if (!(ok = w.wait(&sm.k_full[gn % C::NS], (gn / C::NS) & 1, kErrPrefillKFull)))
+                  break;
+                tc_fence_after();
+                kn_ready = true;
+              }
+              issue_s(t, gj + 1);
+            } else {
+              umma_commit(&sm.o_final[t]);
+            }
           }
+          if (v_ready) umma_commit(&sm.v_empty[s]);
+          if (kn_ready) umma_commit(&sm.k_empty[(gj + 1) % C::NS]);
+          if (j == it.nmax - 2) umma_commit(&sm.q_empty);  // last S MMA issued
         }
-        if (v_ready) umma_commit(&sm.v_empty[s]);
-        if (kn_ready) umma_commit(&sm.k_empty[(j + 1) % C::NS]);
+        for (int t = 0; t < 2; ++t)
+          if (it.n[t] > 0) ++oc[t];
+        g += it.nmax;
       }
       // All MMAs this thread issued must finish before tensor memory is freed.
       umma_commit(&sm.teardown);
       if (!wait_raw(&sm.teardown, 0, globaltimer_ns() + 50000000ull) && p.err)
         atomicOr(p.err, 1u << kErrPrefillTeardown);
     }
-  }  // warps 10, 11: no role
+    // warps 10, 11 and the other lanes: no role
   } else {
-#ifndef ATTN_PREFILL_WARPS10
-    setmaxnreg_inc<224>();
-#endif
+    setmaxnreg_inc<200>();
     // ======================= softmax warpgroups =============================
-    const int t = warp >> 2;           // query tile of this warpgroup
-    const int r = threadIdx.x & 127;   // row within the tile == TMEM lane
+    using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    const int t = warp >> 2;          // query tile of this warpgroup
+    const int r = threadIdx.x & 127;  // row within the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + C::tm_s(t) + lane_base;
     const uint32_t tO = tmem + C::tm_o(t) + lane_base;
-    const int mt = m0 + t * C::BM;
-    const int qi = mt + r;             // query index within the sequence
-    const int nt = n_t[t];
-    const int diag = Lk - Lq;          // bottom-right alignment offset
-
-    float m_use = -INFINITY;  // exp2 subtrahend currently in use (log2 units)
-    float l = 0.0f;           // running denominator w.r.t. m_use
+    int pc = 0, oc = 0;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      ok = __all_sync(0xffffffffu, w.wait(&sm.s_full[t], j & 1, kErrPrefillSFull));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[128];
-      {
-        uint32_t (&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-        uint32_t (&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-        uint32_t (&a2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
-        uint32_t (&a3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
-        tmem_ld32(tS + 0, a0);
-        tmem_ld32(tS + 32, a1);
-        tmem_ld32(tS + 64, a2);
-        tmem_ld32(tS + 96, a3);
-        tmem_ld_wait();
-        reg_fence(sr);
-      }
-      // Raw scores in place; the soft-cap variant turns them into capped
-      // log2-unit scores first, else the scale*log2(e) factor is folded into
-      // the exponent's FMA (CK MakeKargs FAST_EXP2 fold).
-      float* s = reinterpret_cast<float*>(sr);
-      float a_coef = p.scale_log2;
-      if constexpr (SOFTCAP) {
-        tanh128(s, p.scale * p.softcap_inv);  // s <- tanh(scale * s / cap)
-        a_coef = p.softcap * kLog2e;          // capped score in log2 units = a_coef * s
-      }
-      const int j0 = j * C::BN;
-      const bool need_mask =
-          (j0 + C::BN > Lk) || (CAUSAL && (j0 + C::BN - 1 > mt + diag));
-      int lim = 127;
-      if (need_mask) {
-        lim = Lk - 1 - j0;
-        if (CAUSAL) lim = min(lim, qi + diag - j0);
+    for (int rr = 0; ok; ++rr) {
+      const int item = item_of_round(rr);
+      if (item >= p.num_items) break;
+      PrefillItem it;
+      if (!decode_item<C::BM, C::BN, CAUSAL>(p, item, it)) continue;
+      const int mt = it.m0 + t * C::BM;
+      if (mt >= it.Lq) continue;  // this tile has no row
+      const int qi = mt + r;      // query index within the sequence
+      const int nt = it.n[t];
+      const int diag = it.Lk - it.Lq;  // bottom-right alignment offset
+
+      float m_use = -INFINITY;  // exp2 subtrahend currently in use (log2 units)
+      float l = 0.0f;           // running denominator w.r.t. m_use
+      for (int j = 0; j < nt; ++j) {
+        ok = __all_sync(0xffffffffu, w.wait(&sm.s_full[t], pc & 1, kErrPrefillSFull));
+        if (!ok) break;
+        ++pc;
+        tc_fence_after();
+        uint32_t sr[128];
+        {
+          uint32_t (&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+          uint32_t (&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+          uint32_t (&a2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
+          uint32_t (&a3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
+          tmem_ld32(tS + 0, a0);
+          tmem_ld32(tS + 32, a1);
+          tmem_ld32(tS + 64, a2);
+          tmem_ld32(tS + 96, a3);
+          tmem_ld_wait();
+          reg_fence(sr);
+        }
+        // Raw scores in place; the soft-cap variant turns them into tanh
+        // values whose log2-unit score is cap*log2(e)*s, else scale*log2(e)
+        // is folded into the exponent's FMA (CK MakeKargs FAST_EXP2 fold).
+        float* s = reinterpret_cast<float*>(sr);
+        float a_coef = p.scale_log2;
+        if constexpr (SOFTCAP) {
+          tanh128(s, p.scale * p.softcap_inv);
+          a_coef = p.softcap * kLog2e;
+        }
+        const int j0 = j * C::BN;
+        if ((j0 + C::BN > it.Lk) || (CAUSAL && (j0 + C::BN - 1 > mt + diag))) {
+          int lim = it.Lk - 1 - j0;
+          if (CAUSAL) lim = min(lim, qi + diag - j0);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+          for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+        }
+        const float m_new = fmaxf(m_use, max128(s) * a_coef);  // a_coef > 0: order kept
+        float alpha = 1.0f;
+        if (m_new - m_use > 8.0f) {  // false when both are -inf (NaN compare)
+          alpha = ex2_approx(m_use - m_new);
+          m_use = m_new;
+        }
+        const float msub = (m_use == -INFINITY) ? 0.0f : m_use;
+        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f in both lanes
+        uint32_t pk[64];
+        exp_pack_row<BF16>(s, f2_pack(a_coef, a_coef), f2_pack(-msub, -msub), pk, acc2);
+        float r0, r1;
+        f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), r0, r1);
+        l = l * alpha + (r0 + r1);
+        tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        // The P.V MMA of the previous K/V tile finished before this S was
+        // produced (its commit covers every earlier MMA), so O can be
+        // rescaled now.
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c, ov);
+            tmem_ld_wait();
+            reg_fence(ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(tO + c, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[t]);
       }
-      const float m_new = fmaxf(m_use, max128(s) * a_coef);  // a_coef > 0: order kept
-      float alpha = 1.0f;
-      if (m_new - m_use > 8.0f) {  // false when both are -inf (NaN compare)
-        alpha = ex2_approx(m_use - m_new);
-        m_use = m_new;
+      if (!ok) break;
+
+      // ---- epilogue: O = O / l, LSE = ln(l) + m (FA2 final rescale; FA3 store)
+      bool have_o = false;
+      if (nt > 0) {
+        have_o = __all_sync(0xffffffffu, w.wait(&sm.o_final[t], oc & 1, kErrPrefillOFinal));
+        ++oc;
+        if (!have_o) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
       }
       const float msub = (m_use == -INFINITY) ? 0.0f : m_use;
-      uint64_t acc2[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc2[i] = 0ull;  // +0.0f in both lanes
-      uint32_t pk[64];
-      const uint64_t a2 = f2_pack(a_coef, a_coef), nb2 = f2_pack(-msub, -msub);
-      if (need_mask) exp_pack_row<BF16, true>(s, a2, nb2, lim, pk, acc2);
-      else exp_pack_row<BF16, false>(s, a2, nb2, lim, pk, acc2);
-      float r0, r1;
-      f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), r0, r1);
-      l = l * alpha + (r0 + r1);
-      tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      // The P.V MMA of the previous tile finished before this S was produced
-      // (its commit covers every earlier MMA), so O can be rescaled now.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+      float mfin = msub, ltot = l, oscale;
+      if (p.sink != nullptr) {
+        const float sl = p.sink[it.h] * kLog2e;
+        if (l > 0.0f) {
+          mfin = fmaxf(msub, sl);
+          const float a = ex2_approx(msub - mfin);
+          ltot = l * a + ex2_approx(sl - mfin);
+          oscale = a / ltot;
+        } else {
+          mfin = sl;
+          ltot = 1.0f;
+          oscale = 0.0f;
+        }
+      } else {
+        oscale = (l > 0.0f) ? 1.0f / l : 0.0f;
+      }
+      const bool row_ok = qi < it.Lq;
+      if (row_ok && p.lse != nullptr) {
+        const float lse = (ltot > 0.0f) ? (mfin + __log2f(ltot)) * kLn2 : -INFINITY;
+        p.lse[it.b * p.lse_batch + it.h * p.lse_head + it.rq0 + qi] = lse;
+      }
+      T* orow = reinterpret_cast<T*>(p.o) + it.b * p.o_batch + it.h * p.o_head +
+                static_cast<int64_t>(it.rq0 + qi) * p.o_row;
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+      if (have_o) {
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t ov[32];
           tmem_ld32(tO + c, ov);
           tmem_ld_wait();
           reg_fence(ov);
+          if (row_ok) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(tO + c, ov);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.p_full[t]);
-    }
-
-    // ---- epilogue: O = O / l, LSE = ln(l) + m (FA2 final rescale; FA3 store) --
-    const bool have_o = __all_sync(
-        0xffffffffu, ok && nt > 0 && w.wait(&sm.o_final[t], 0, kErrPrefillOFinal));
-    if (have_o) tc_fence_after();
-    const float msub = (m_use == -INFINITY) ? 0.0f : m_use;
-    float mfin = msub, ltot = l, oscale;
-    if (p.sink != nullptr) {
-      const float sl = p.sink[h] * kLog2e;
-      if (l > 0.0f) {
-        mfin = fmaxf(msub, sl);
-        const float a = ex2_approx(msub - mfin);
-        ltot = l * a + ex2_approx(sl - mfin);
-        oscale = a / ltot;
-      } else {
-        mfin = sl;
-        ltot = 1.0f;
-        oscale = 0.0f;
-      }
-    } else {
-      oscale = (l > 0.0f) ? 1.0f / l : 0.0f;
-    }
-    const bool row_ok = (qi < Lq) && (ok || nt == 0);
-    if (row_ok && p.lse != nullptr) {
-      const float lse = (ltot > 0.0f) ? (mfin + __log2f(ltot)) * kLn2 : -INFINITY;
-      p.lse[b * p.lse_batch + h * p.lse_head + rq0 + qi] = lse;
-    }
-    using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-    T* orow = reinterpret_cast<T*>(p.o) + b * p.o_batch + h * p.o_head +
-              static_cast<int64_t>(rq0 + qi) * p.o_row;
-    if (have_o) {
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t w4[4];
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t ov[32];
-        tmem_ld32(tO + c, ov);
-        tmem_ld_wait();
-        reg_fence(ov);
-        if (row_ok) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = __uint_as_float(ov[2 * i]) * oscale;
-            const float bb = __uint_as_float(ov[2 * i + 1]) * oscale;
-            pk[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
+              for (int i = 0; i < 4; ++i) {
+                const float a = __uint_as_float(ov[8 * q4 + 2 * i]) * oscale;
+                const float bb = __uint_as_float(ov[8 * q4 + 2 * i + 1]) * oscale;
+                w4[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
+              }
+              dst[c / 8 + q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
           }
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
-      }
-    } else if (row_ok) {
-      uint4* dst = reinterpret_cast<uint4*>(orow);
+        // O_t may now be overwritten by the next item's first P.V.
+        tc_fence_before();
+        mbar_arrive(&sm.o_free[t]);
+      } else if (row_ok) {
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+      }
     }
   }
 
@@ -539,8 +564,8 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream
 
 cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool causal,
                            bool softcap, cudaStream_t stream, char* name, size_t name_len) {
-  snprintf(name, name_len, "attn_prefill_tcgen05_d%d_%s_%s_%s_m256n128", d, bf16 ? "bf16" : "f16",
-           causal ? "causal" : "nomask", softcap ? "softcap" : "nocap");
+  snprintf(name, name_len, "attn_prefill_tcgen05_d%d_%s_%s_%s_m256n128_persistent", d,
+           bf16 ? "bf16" : "f16", causal ? "causal" : "nomask", softcap ? "softcap" : "nocap");
 #define ATTN_PREFILL_CASE(D_, B_, C_, S_)                                        \
   if (d == D_ && bf16 == B_ && causal == C_ && softcap == S_)                    \
     return launch_prefill_t<D_, B_, C_, S_>(p, grid, stream);
