@@ -28,6 +28,10 @@
  *   Composable Kernel, operator() (mask from the left/right window,
  *     MASK_FROM_TOP_LEFT vs. the default bottom-right alignment):
  *     causal bottom-right keeps key j for query i iff j <= i + (Lk - Lq).
+ *     The window mask (window_size_left / window_size_right of the same
+ *     kargs, same bottom-right alignment) keeps j iff
+ *       i + (Lk - Lq) - left <= j <= i + (Lk - Lq) + right,
+ *     a negative size meaning unbounded on that side; causal is right = 0.
  *   FlashAttention-3 hopper/epilogue_fwd.hpp, CollectiveEpilogueFwd::store_zero:
  *     a row with no key to attend to gets O = 0 and LSE = -inf (with a sink:
  *     O = 0 and LSE = sigma).
@@ -77,7 +81,7 @@
  *   o: [d] output row; *lse: output.
  * Returns nothing; empty rows follow the store_zero convention. */
 static void row_forward(const double* q, const double* k, const double* v, long kvstride,
-                        int Lq, int Lk, int qi, int d, double scale, int causal,
+                        int Lq, int Lk, int qi, int d, double scale, int causal, int wl, int wr,
                         double softcap, int has_sink, double sink,
                         double* s_row, double* p_row, unsigned char* keep,
                         double* o, double* lse)
@@ -96,10 +100,14 @@ static void row_forward(const double* q, const double* k, const double* v, long 
             else s = softcap * tanh(s / softcap);
         }
         s_row[j] = s;
-        /* bottom-right causal alignment */
-        long lim = (long)qi + (long)(Lk - Lq);
+        /* bottom-right alignment of the causal and window bounds */
+        const long diag = (long)qi + (long)(Lk - Lq);
+        long lim = diag;
         if (MUTANT(4)) lim = qi;                           /* top-left instead */
-        keep[j] = (unsigned char)(!causal || (long)j <= lim);
+        int kept = !causal || (long)j <= lim;
+        if (wr >= 0 && (long)j > diag + wr) kept = 0;
+        if (wl >= 0 && (long)j < diag - wl + (MUTANT(9) ? 1 : 0)) kept = 0; /* MUTANT 9: off by one */
+        keep[j] = (unsigned char)kept;
     }
 
     int any = 0;
@@ -149,8 +157,8 @@ static int kv_head_of(int h, int Hq, int Hkv)
 int oracle_attn_dense(const double* q, const double* k, const double* v,
                       double* o, double* lse,
                       int B, int Hq, int Hkv, int Lq, int Lk, int d,
-                      double scale, int causal, double softcap, const double* sink,
-                      double* s_out, double* p_out)
+                      double scale, int causal, int wl, int wr, double softcap,
+                      const double* sink, double* s_out, double* p_out)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Lq < 0 || Lk < 0 || d <= 0) return 1;
     long nbh = (long)B * Hq;
@@ -165,7 +173,7 @@ int oracle_attn_dense(const double* q, const double* k, const double* v,
         double* p_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
         unsigned char* keep = (unsigned char*)malloc(Lk > 0 ? Lk : 1);
         for (int i = 0; i < Lq; ++i) {
-            row_forward(qh + (long)i * d, kh, vh, d, Lq, Lk, i, d, scale, causal, softcap,
+            row_forward(qh + (long)i * d, kh, vh, d, Lq, Lk, i, d, scale, causal, wl, wr, softcap,
                         sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
                         o + (((long)b * Hq + h) * Lq + i) * d,
                         lse + ((long)b * Hq + h) * Lq + i);
@@ -182,7 +190,8 @@ int oracle_attn_varlen(const double* q, const double* k, const double* v,
                        double* o, double* lse,
                        const int32_t* cu_q, const int32_t* cu_k,
                        int B, int Hq, int Hkv, int d,
-                       double scale, int causal, double softcap, const double* sink)
+                       double scale, int causal, int wl, int wr, double softcap,
+                       const double* sink)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0) return 1;
     int total_q = cu_q[B];
@@ -201,8 +210,8 @@ int oracle_attn_varlen(const double* q, const double* k, const double* v,
         const double* vh = v + (long)k0 * kvstride + (long)hk * d;
         for (int i = 0; i < Lq; ++i) {
             long row = q0 + i;
-            row_forward(q + (row * Hq + h) * d, kh, vh, kvstride, Lq, Lk, i, d, scale, causal,
-                        softcap, sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
+            row_forward(q + (row * Hq + h) * d, kh, vh, kvstride, Lq, Lk, i, d, scale, causal, wl,
+                        wr, softcap, sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
                         o + (row * Hq + h) * d, lse + (long)h * total_q + row);
         }
         free(s_row); free(p_row); free(keep);
@@ -227,7 +236,8 @@ int oracle_attn_paged(const double* q, const double* k_pool, const double* v_poo
                       const int32_t* block_table, const int32_t* seqlens_k,
                       double* o, double* lse,
                       int B, int Lq, int Hq, int Hkv, int d, int page, int max_pages,
-                      double scale, int causal, double softcap, const double* sink)
+                      double scale, int causal, int wl, int wr, double softcap,
+                      const double* sink)
 {
     if (B < 0 || Lq < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || page <= 0) return 1;
     long nbh = (long)B * Hq;
@@ -245,7 +255,7 @@ int oracle_attn_paged(const double* q, const double* k_pool, const double* v_poo
         unsigned char* keep = (unsigned char*)malloc(Lk > 0 ? Lk : 1);
         for (int i = 0; i < Lq; ++i) {
             row_forward(q + (((long)b * Lq + i) * Hq + h) * d, kg, vg, d, Lq, Lk, i, d, scale,
-                        causal, softcap, sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
+                        causal, wl, wr, softcap, sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
                         o + (((long)b * Lq + i) * Hq + h) * d, lse + ((long)b * Hq + h) * Lq + i);
         }
         free(kg); free(vg); free(s_row); free(p_row); free(keep);
@@ -263,7 +273,7 @@ int oracle_attn_paged_partials(const double* q, const double* k_pool, const doub
                                double* o_part, double* lse_part,
                                int B, int Lq, int Hq, int Hkv, int d, int page, int max_pages,
                                int num_splits, int chunk_pages,
-                               double scale, int causal, double softcap)
+                               double scale, int causal, int wl, int wr, double softcap)
 {
     if (B < 0 || Lq < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || page <= 0 ||
         num_splits <= 0 || chunk_pages <= 0) return 1;
@@ -302,7 +312,7 @@ int oracle_attn_paged_partials(const double* q, const double* k_pool, const doub
                 int ishift = (int)(i + (Lk - Lks) - j0);
                 /* row_forward evaluates j <= ishift + (Lks - Lq) */
                 row_forward(q + (((long)b * Lq + i) * Hq + h) * d, kg + j0 * d, vg + j0 * d, d,
-                            Lq, Lks, ishift, d, scale, causal, softcap, 0, 0.0,
+                            Lq, Lks, ishift, d, scale, causal, wl, wr, softcap, 0, 0.0,
                             s_row, p_row, keep, orow, lrow);
             }
         }

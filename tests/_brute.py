@@ -9,11 +9,16 @@ alignment and empty rows stated in the oracle.  No numpy, no shared code.
 import math
 
 
-def row(qv, keys, vals, scale, qi, Lq, causal, softcap, sink):
+def row(qv, keys, vals, scale, qi, Lq, causal, softcap, sink, window=(-1, -1)):
     Lk = len(keys)
     scores = []
+    diag = qi + (Lk - Lq)
     for j in range(Lk):
-        if causal and j > qi + (Lk - Lq):
+        if causal and j > diag:
+            continue
+        if window[1] >= 0 and j > diag + window[1]:
+            continue
+        if window[0] >= 0 and j < diag - window[0]:
             continue
         s = scale * math.fsum(a * b for a, b in zip(qv, keys[j]))
         if softcap > 0:
@@ -32,7 +37,7 @@ def row(qv, keys, vals, scale, qi, Lq, causal, softcap, sink):
     return out, lse
 
 
-def dense(q, k, v, scale, causal=False, softcap=0.0, sink=None):
+def dense(q, k, v, scale, causal=False, softcap=0.0, sink=None, window=(-1, -1)):
     """q [B][Hq][Lq][d], k/v [B][Hkv][Lk][d] nested lists -> (o, lse)."""
     B, Hq = len(q), len(q[0])
     Hkv = len(k[0])
@@ -43,7 +48,7 @@ def dense(q, k, v, scale, causal=False, softcap=0.0, sink=None):
         for h in range(Hq):
             Lq = len(q[b][h])
             rows = [row(q[b][h][i], k[b][h // g], v[b][h // g], scale, i, Lq, causal, softcap,
-                        None if sink is None else sink[h]) for i in range(Lq)]
+                        None if sink is None else sink[h], window) for i in range(Lq)]
             o[b][h] = [r[0] for r in rows]
             lse[b][h] = [r[1] for r in rows]
     return o, lse

@@ -309,10 +309,43 @@ def pin_varlen_equals_per_sequence(mutant=0):
         _close(lse[:, cu_q[b]:cu_q[b + 1]], ld[0], 0.0, "varlen LSE")
 
 
+def pin_window(mutant=0):
+    """Sliding window (bottom-right aligned, CK window_size_left/right):
+    brute force agrees; (-1,-1) is no mask; (-1,0) is causal; (0,0) keeps only
+    key i + (Lk - Lq), so O_i = V[i + Lk - Lq] and LSE_i is that one score."""
+    r = _rng(14)
+    for (Lq, Lk, wl, wr, causal, cap, sink) in ((6, 9, 2, 1, False, 0.0, False),
+                                               (9, 6, 3, 0, True, 0.0, True),
+                                               (5, 5, 0, 2, False, 1.5, False),
+                                               (4, 11, 1, -1, False, 0.0, True)):
+        q = r.standard_normal((1, 2, Lq, 4))
+        k = r.standard_normal((1, 1, Lk, 4))
+        v = r.standard_normal((1, 1, Lk, 4))
+        sk = r.standard_normal(2) if sink else None
+        o, lse = oracle.attn_dense(q, k, v, 0.6, causal, cap, sk, mutant=mutant, window=(wl, wr))
+        bo, bl = _brute.dense(q.tolist(), k.tolist(), v.tolist(), 0.6, causal, cap,
+                              None if sk is None else sk.tolist(), window=(wl, wr))
+        _close(o, np.array(bo), 1e-12, f"window brute O {Lq, Lk, wl, wr}")
+        _close(lse, np.array(bl), 1e-12, f"window brute LSE {Lq, Lk, wl, wr}")
+    q = r.standard_normal((1, 2, 7, 4))
+    k = r.standard_normal((1, 2, 10, 4))
+    v = r.standard_normal((1, 2, 10, 4))
+    o0, l0 = oracle.attn_dense(q, k, v, 0.5, mutant=mutant)
+    o1, l1 = oracle.attn_dense(q, k, v, 0.5, mutant=mutant, window=(-1, -1))
+    _close(o1, o0, 0.0, "window unbounded")
+    oc, lc = oracle.attn_dense(q, k, v, 0.5, causal=True, mutant=mutant)
+    o2, l2 = oracle.attn_dense(q, k, v, 0.5, mutant=mutant, window=(-1, 0))
+    _close(o2, oc, 0.0, "window (-1, 0) is causal")
+    _close(l2, lc, 0.0, "window (-1, 0) is causal, LSE")
+    o3, l3 = oracle.attn_dense(q, k, v, 0.5, mutant=mutant, window=(0, 0))
+    _close(o3, v[:, :, 3:10], 0.0, "width-one window")
+    _close(l3, 0.5 * np.einsum("bhid,bhid->bhi", q, k[:, :, 3:10]), 1e-14, "width-one LSE")
+
+
 PINS = [pin_golden, pin_rows_sum_to_one, pin_identical_keys, pin_one_hot, pin_lse_fsum,
         pin_causal_row0, pin_empty_rows, pin_brute_force, pin_softcap_limits, pin_sink_limits,
         pin_gqa_equals_repeated_mha, pin_paged_equals_contiguous, pin_splits_combine_to_unsplit,
-        pin_varlen_equals_per_sequence]
+        pin_varlen_equals_per_sequence, pin_window]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
