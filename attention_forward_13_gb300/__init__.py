@@ -21,7 +21,8 @@ from . import _lib
 
 __all__ = ["attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_splitkv_combine",
            "attn_paged_workspace_bytes", "attn_paged_auto_splits", "attn_device_error",
-           "attn_selftest_timeout", "attn_last_kernel_name", "AttnError", "library"]
+           "attn_selftest_timeout", "attn_last_kernel_name", "attn_paged_window_pages",
+           "attn_fwd_paged_noalloc", "AttnError", "library"]
 
 
 class AttnError(RuntimeError):
@@ -56,12 +57,15 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _opts(scale, causal, softcap, sink):
+def _opts(scale, causal, softcap, sink, window=None):
     o = _lib.attn_opts()
     o.scale = float(scale) if scale is not None else 0.0
     o.causal = 1 if causal else 0
     o.softcap = float(softcap) if softcap else 0.0
     o.sink = sink.data_ptr() if sink is not None else None
+    if window is not None:
+        o.use_window = 1
+        o.window_left, o.window_right = int(window[0]), int(window[1])
     return o
 
 
@@ -88,9 +92,10 @@ def _check_sink(sink, Hq, device):
 
 
 def attn_fwd(q, k, v, o=None, lse=True, causal=False, scale=None, softcap=0.0, sink=None,
-             stream=None):
+             stream=None, window=None):
     """Dense attention.  q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] (any strides with d-stride 1).
-    Returns (o [B,Hq,Lq,d], lse fp32 [B,Hq,Lq] or None)."""
+    ``window`` = (left, right) keeps keys i+Lk-Lq-left <= j <= i+Lk-Lq+right (a
+    negative side is unbounded).  Returns (o [B,Hq,Lq,d], lse fp32 [B,Hq,Lq] or None)."""
     B, Hq, Lq, d = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     if o is None:
@@ -101,7 +106,7 @@ def attn_fwd(q, k, v, o=None, lse=True, causal=False, scale=None, softcap=0.0, s
     elif isinstance(lse, torch.Tensor):
         lse_t = lse
     sink = _check_sink(sink, Hq, q.device)
-    opts = _opts(scale, causal, softcap, sink)
+    opts = _opts(scale, causal, softcap, sink, window)
     st = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, Hq, Hkv, Lq, Lk,
                             d, _dtype_code(q), _strides_bhld(q), _strides_bhld(k),
                             _strides_bhld(v), _strides_bhld(o), ctypes.byref(opts),
@@ -111,7 +116,7 @@ def attn_fwd(q, k, v, o=None, lse=True, causal=False, scale=None, softcap=0.0, s
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, o=None, lse=True,
-                    causal=False, scale=None, softcap=0.0, sink=None, stream=None):
+                    causal=False, scale=None, softcap=0.0, sink=None, stream=None, window=None):
     """Group mode.  q [total_q,Hq,d], k/v [total_k,Hkv,d], cu_seqlens int32 [B+1] on the
     device.  Returns (o [total_q,Hq,d], lse fp32 [Hq,total_q] or None)."""
     total_q, Hq, d = q.shape
@@ -128,7 +133,7 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, o=None, l
     elif isinstance(lse, torch.Tensor):
         lse_t = lse
     sink = _check_sink(sink, Hq, q.device)
-    opts = _opts(scale, causal, softcap, sink)
+    opts = _opts(scale, causal, softcap, sink, window)
     st = library().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t),
                                    _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, total_q, total_k,
                                    int(max_seqlen_q), Hq, Hkv, d, _dtype_code(q),
@@ -146,9 +151,16 @@ def attn_paged_auto_splits(B, Hkv, max_pages_per_seq) -> int:
     return int(library().attn_paged_auto_splits(B, Hkv, max_pages_per_seq))
 
 
+def attn_paged_window_pages(Lq, page_size, max_pages_per_seq, window=None, causal=False) -> int:
+    """Pages of one sequence the paged split layout tiles (W of attn_fwd_paged)."""
+    opts = _opts(None, causal, 0.0, None, window)
+    return int(library().attn_paged_window_pages(Lq, page_size, max_pages_per_seq,
+                                                 ctypes.byref(opts)))
+
+
 def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=None, lse=True,
                    causal=False, scale=None, softcap=0.0, sink=None, workspace=None,
-                   stream=None):
+                   stream=None, window=None):
     """Paged KV.  q [B,Lq,Hq,d], pools [num_pages,page,Hkv,d], block_table int32
     [B,max_pages], seqlens_k int32 [B] (all on the device, contiguous).
     Returns (o [B,Lq,Hq,d], lse fp32 [B,Hq,Lq] or None)."""
@@ -159,7 +171,8 @@ def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=No
         if not t.is_contiguous():
             raise ValueError("paged inputs must be contiguous")
     if num_splits == 0:
-        num_splits = attn_paged_auto_splits(B, Hkv, max_pages)
+        num_splits = attn_paged_auto_splits(
+            B, Hkv, attn_paged_window_pages(Lq, page, max_pages, window, causal))
     if o is None:
         o = torch.empty((B, Lq, Hq, d), dtype=q.dtype, device=q.device)
     lse_t = None
@@ -176,7 +189,7 @@ def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=No
         o_part = workspace[: num_splits * rows * d]
         lse_part = workspace[num_splits * rows * d: need]
     sink = _check_sink(sink, Hq, q.device)
-    opts = _opts(scale, causal, softcap, sink)
+    opts = _opts(scale, causal, softcap, sink, window)
     st = library().attn_fwd_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
                                   _ptr(seqlens_k), _ptr(o), _ptr(lse_t), B, Lq, Hq, Hkv, d,
                                   _dtype_code(q), page, num_pages, max_pages, num_splits,
@@ -188,7 +201,7 @@ def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=No
 
 def attn_fwd_paged_noalloc(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=None,
                            lse=True, causal=False, scale=None, softcap=0.0, sink=None,
-                           stream=None):
+                           stream=None, window=None):
     """attn_fwd_paged for callers that cannot allocate device scratch: the split
     partials live in a fixed 16 MiB array inside the library (shared by all
     calls on a GPU; calls overlapping on the GPU race).  Outputs are allocated
@@ -203,7 +216,7 @@ def attn_fwd_paged_noalloc(q, k_pool, v_pool, block_table, seqlens_k, num_splits
     elif isinstance(lse, torch.Tensor):
         lse_t = lse
     sink = _check_sink(sink, Hq, q.device)
-    opts = _opts(scale, causal, softcap, sink)
+    opts = _opts(scale, causal, softcap, sink, window)
     st = library().attn_fwd_paged_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
                                           _ptr(seqlens_k), _ptr(o), _ptr(lse_t), B, Lq, Hq, Hkv,
                                           d, _dtype_code(q), page, num_pages,

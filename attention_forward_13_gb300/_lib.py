@@ -18,7 +18,8 @@ class attn_strides(ctypes.Structure):
 
 class attn_opts(ctypes.Structure):
     _fields_ = [("scale", ctypes.c_float), ("causal", ctypes.c_int), ("softcap", ctypes.c_float),
-                ("sink", ctypes.c_void_p)]
+                ("sink", ctypes.c_void_p), ("use_window", ctypes.c_int),
+                ("window_left", ctypes.c_int), ("window_right", ctypes.c_int)]
 
 
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
@@ -28,7 +29,7 @@ ATTN_F16, ATTN_BF16 = 0, 1
 EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_splitkv_combine",
            "attn_paged_workspace_bytes", "attn_paged_auto_splits", "attn_status_string",
            "attn_last_kernel_name", "attn_device_error", "attn_selftest_timeout",
-           "attn_fwd_paged_noalloc")
+           "attn_fwd_paged_noalloc", "attn_paged_window_pages")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
@@ -53,6 +54,8 @@ def _declare(lib):
     lib.attn_paged_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_paged_auto_splits.argtypes = [_I, _I, _I]
     lib.attn_paged_auto_splits.restype = _I
+    lib.attn_paged_window_pages.argtypes = [_I, _I, _I, O]
+    lib.attn_paged_window_pages.restype = _I
     lib.attn_status_string.argtypes = [_I]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_last_kernel_name.argtypes = []

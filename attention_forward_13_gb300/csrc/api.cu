@@ -108,6 +108,18 @@ float resolve_scale(const attn_opts* o, int d) {
   return (o != nullptr && o->scale > 0.0f) ? o->scale : 1.0f / sqrtf(static_cast<float>(d));
 }
 
+// Effective key bounds (negative = unbounded); causal is a right bound of 0.
+void resolve_window(const attn_opts* opts, int* wl, int* wr) {
+  *wl = -1;
+  *wr = -1;
+  if (opts == nullptr) return;
+  if (opts->use_window) {
+    *wl = opts->window_left < 0 ? -1 : opts->window_left;
+    *wr = opts->window_right < 0 ? -1 : opts->window_right;
+  }
+  if (opts->causal) *wr = 0;  // any window_right >= 0 is looser than causal
+}
+
 void fill_common(PrefillParams& p, const attn_opts* opts, int d) {
   const float scale = resolve_scale(opts, d);
   p.scale = scale;
@@ -116,6 +128,7 @@ void fill_common(PrefillParams& p, const attn_opts* opts, int d) {
   p.softcap = cap;
   p.softcap_inv = cap > 0.0f ? 1.0f / cap : 0.0f;
   p.sink = opts != nullptr ? opts->sink : nullptr;
+  resolve_window(opts, &p.win_left, &p.win_right);
   p.timeout_ns = kTimeoutNs;
 }
 
@@ -256,10 +269,10 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.num_m_blocks = (Lq + 255) / 256;
   p.err = err;
   fill_common(p, opts, d);
-  const bool causal = opts != nullptr && opts->causal != 0;
+  const bool masked = p.win_left >= 0 || p.win_right >= 0;
   p.num_items = p.num_m_blocks * B * Hq;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
-  return finish_launch(launch_prefill(p, grid, d, bf16, causal, p.softcap > 0.0f,
+  return finish_launch(launch_prefill(p, grid, d, bf16, masked, p.softcap > 0.0f,
                                       static_cast<cudaStream_t>(stream), g_last_name,
                                       sizeof(g_last_name)));
 }
@@ -333,10 +346,10 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   p.num_m_blocks = (max_seqlen_q + 255) / 256;
   p.err = err;
   fill_common(p, opts, d);
-  const bool causal = opts != nullptr && opts->causal != 0;
+  const bool masked = p.win_left >= 0 || p.win_right >= 0;
   p.num_items = p.num_m_blocks * B * Hq;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
-  return finish_launch(launch_prefill(p, grid, d, bf16, causal, p.softcap > 0.0f,
+  return finish_launch(launch_prefill(p, grid, d, bf16, masked, p.softcap > 0.0f,
                                       static_cast<cudaStream_t>(stream), g_last_name,
                                       sizeof(g_last_name)));
 }
@@ -345,6 +358,14 @@ size_t attn_paged_workspace_bytes(int B, int Lq, int Hq, int d, int num_splits) 
   if (B <= 0 || Lq <= 0 || Hq <= 0 || d <= 0 || num_splits <= 1) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * Lq;
   return static_cast<size_t>(num_splits) * rows * (static_cast<size_t>(d) + 1) * sizeof(float);
+}
+
+int attn_paged_window_pages(int Lq, int page_size, int max_pages_per_seq, const attn_opts* opts) {
+  int wl = -1, wr = -1;
+  resolve_window(opts, &wl, &wr);
+  if (wl < 0 || Lq < 0 || page_size <= 0 || max_pages_per_seq <= 0) return max_pages_per_seq;
+  const int64_t w = (static_cast<int64_t>(Lq) + wl + page_size - 1) / page_size + 1;
+  return w < max_pages_per_seq ? static_cast<int>(w) : max_pages_per_seq;
 }
 
 int attn_paged_auto_splits(int B, int Hkv, int max_pages_per_seq) {
@@ -419,7 +440,8 @@ attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool
       (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return ATTN_ERR_INVALID;
   if (B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
-  if (num_splits == 0) num_splits = attn_paged_auto_splits(B, Hkv, max_pages_per_seq);
+  const int win_pages = attn_paged_window_pages(Lq, page_size, max_pages_per_seq, opts);
+  if (num_splits == 0) num_splits = attn_paged_auto_splits(B, Hkv, win_pages);
   if (num_splits > 1 && (o_partial == nullptr || lse_partial == nullptr ||
                          !aligned16(o_partial) || (reinterpret_cast<uintptr_t>(lse_partial) & 3u)))
     return ATTN_ERR_INVALID;
@@ -452,13 +474,13 @@ attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool
   p.num_pages = num_pages;
   p.max_pages = max_pages_per_seq;
   p.num_splits = num_splits;
-  p.chunk_pages = (max_pages_per_seq + num_splits - 1) / num_splits;
+  p.chunk_pages = (win_pages + num_splits - 1) / num_splits;
   const float scale = resolve_scale(opts, d);
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.softcap = (opts != nullptr && opts->softcap > 0.0f) ? opts->softcap : 0.0f;
   p.softcap_inv = p.softcap > 0.0f ? 1.0f / p.softcap : 0.0f;
-  p.causal = (opts != nullptr && opts->causal != 0) ? 1 : 0;
+  resolve_window(opts, &p.win_left, &p.win_right);
   p.err = err;
   p.timeout_ns = kTimeoutNs;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -51,6 +51,10 @@ struct PrefillParams {
   float scale;                     // plain scale (soft-cap path)
   float softcap;                   // cap (> 0 when the soft-cap variant runs)
   float softcap_inv;               // 1 / cap
+  // Key bounds of query row i (bottom-right aligned): i + Lk - Lq - win_left
+  // <= j <= i + Lk - Lq + win_right; a negative bound is unbounded.  Causal
+  // masking is win_right = 0.  Only read by the masked instantiations.
+  int win_left, win_right;
   unsigned int* err;
   uint64_t timeout_ns;
 };
@@ -69,7 +73,7 @@ struct DecodeParams {
   const float* sink; // [Hq] or nullptr (used only when num_splits == 1)
   int B, Lq, Hq, Hkv, page_size, num_pages, max_pages, num_splits, chunk_pages;
   float scale_log2, scale, softcap, softcap_inv;
-  int causal;
+  int win_left, win_right;  // as in PrefillParams (causal is win_right = 0)
   unsigned int* err;
   uint64_t timeout_ns;
 };

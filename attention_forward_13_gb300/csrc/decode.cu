@@ -135,7 +135,11 @@ __global__ void __launch_bounds__(192, 2)
   const int L = p.seqlens_k[b];
   const int P = p.page_size;
   const int pages_b = (L + P - 1) / P;
-  const int pg0 = split * p.chunk_pages;
+  // With a left window the splits tile only the pages holding kept keys:
+  // every row's right bound reaches the last key, the first row's left bound
+  // is the lowest.
+  const int k_lo = p.win_left >= 0 ? max(0, L - p.Lq - p.win_left) : 0;
+  const int pg0 = k_lo / P + split * p.chunk_pages;
   const int pg1 = min(pg0 + p.chunk_pages, pages_b);
   const int k0 = pg0 * P;
   const int k1 = min(pg1 * P, L);
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(192, 2)
       m_use[r] = -INFINITY;
       lpart[r] = 0.0f;
     }
-    const int diag = L - p.Lq;  // bottom-right causal offset within the sequence
+    const int diag = L - p.Lq;  // bottom-right mask offset within the sequence
     // Every thread runs every iteration and every named barrier even after a
     // timeout (waits then return at once), so the four warps never part ways
     // at a barrier.
@@ -385,7 +389,8 @@ __global__ void __launch_bounds__(192, 2)
           s *= p.scale_log2;
         }
         bool valid = (key < k1) && (r < R);
-        if (p.causal) valid = valid && (key <= (r / g) + diag);
+        if (p.win_right >= 0) valid = valid && (key <= (r / g) + diag + p.win_right);
+        if (p.win_left >= 0) valid = valid && (key >= (r / g) + diag - p.win_left);
         x[r] = valid ? s : -INFINITY;
       }
       const float wmax = butterfly16<true>(x);

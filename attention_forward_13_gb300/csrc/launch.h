@@ -8,7 +8,7 @@
 namespace attn {
 
 // grid = number of CTAs; name receives the kernel's trait string.
-cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool causal,
+cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool masked,
                            bool softcap, cudaStream_t stream, char* name, size_t name_len);
 
 cudaError_t launch_decode(const DecodeParams& p, int d, bool bf16, bool softcap, int rows,

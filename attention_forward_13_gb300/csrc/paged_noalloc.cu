@@ -70,7 +70,8 @@ extern "C" attn_status attn_fwd_paged_noalloc(const void* q, const void* k_pool,
   // Split count: an explicit count must fit the scratch; the automatic choice
   // is lowered until it fits (one split needs no scratch at all).
   if (num_splits == 0) {
-    num_splits = attn_paged_auto_splits(B, Hkv, max_pages_per_seq);
+    num_splits = attn_paged_auto_splits(
+        B, Hkv, attn_paged_window_pages(Lq, page_size, max_pages_per_seq, opts));
     while (num_splits > 1 &&
            attn_paged_workspace_bytes(B, Lq, Hq, d, num_splits) > ATTN_NOALLOC_SCRATCH_BYTES)
       --num_splits;

@@ -137,19 +137,24 @@ __device__ __forceinline__ bool wait_raw(uint64_t* bar, uint32_t parity, uint64_
 // (batch, query head) against all of its keys.
 struct PrefillItem {
   int b, h, hk, rq0, rk0, bcoord, Lq, Lk, m0;
-  int n[2];  // K/V tiles needed by query tile 0 / 1 (0: no key, or no row)
-  int nmax;
+  int jb;     // first K/V tile of the item
+  int cnt;    // K/V tiles streamed for the item (0: nothing to compute)
+  int ub[2];  // query tile t takes part in steps [ub[t], ue[t]) of the item
+  int ue[2];
 };
 
-// Item index -> coordinates.  Causal problems list the heaviest query blocks
+// Item index -> coordinates.  Masked problems list the heaviest query blocks
 // first (Composable Kernel GetTileIndex reverses the m-tile order when
 // masking).  Returns false when the block starts past the sequence end.
-template <int BM, int BN, bool CAUSAL>
+// Key bounds per query row i (bottom-right aligned, Composable Kernel mask
+// from the left/right window): i + (Lk - Lq) - win_left <= j <= i + (Lk - Lq)
+// + win_right, a negative bound meaning unbounded; causal is win_right = 0.
+template <int BM, int BN, bool MASK>
 __device__ __forceinline__ bool decode_item(const PrefillParams& p, int item, PrefillItem& it) {
   const int nbh = p.B * p.Hq;
   const int mb_i = item / nbh;
   const int bh = item - mb_i * nbh;
-  const int mb = CAUSAL ? (p.num_m_blocks - 1 - mb_i) : mb_i;
+  const int mb = MASK ? (p.num_m_blocks - 1 - mb_i) : mb_i;
   it.h = bh % p.Hq;
   it.b = bh / p.Hq;
   it.hk = it.h / (p.Hq / p.Hkv);
@@ -172,18 +177,33 @@ __device__ __forceinline__ bool decode_item(const PrefillParams& p, int item, Pr
   }
   it.m0 = mb * 2 * BM;
   if (it.m0 >= it.Lq) return false;
+  const int diag = it.Lk - it.Lq;
+  int tb[2], te[2];  // K/V tile range [tb, te) of each query tile
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int mt = it.m0 + t * BM;
-    if (mt >= it.Lq) {
-      it.n[t] = 0;
-    } else {
+    tb[t] = te[t] = 0;
+    if (mt < it.Lq) {
       const int last = min(mt + BM - 1, it.Lq - 1);
-      const int kend = CAUSAL ? min(it.Lk, last + (it.Lk - it.Lq) + 1) : it.Lk;
-      it.n[t] = kend > 0 ? (kend + BN - 1) / BN : 0;
+      int kend = it.Lk, kbeg = 0;  // keys [kbeg, kend) some row of the tile keeps
+      if (MASK && p.win_right >= 0) kend = min(it.Lk, last + diag + p.win_right + 1);
+      if (MASK && p.win_left >= 0) kbeg = max(0, mt + diag - p.win_left);
+      if (kend > kbeg) {
+        tb[t] = kbeg / BN;
+        te[t] = (kend + BN - 1) / BN;
+      }
     }
   }
-  it.nmax = max(it.n[0], it.n[1]);
+  const bool has0 = te[0] > tb[0], has1 = te[1] > tb[1];
+  it.jb = has0 ? (has1 ? min(tb[0], tb[1]) : tb[0]) : tb[1];
+  const int je = max(has0 ? te[0] : 0, has1 ? te[1] : 0);
+  it.cnt = (has0 || has1) ? je - it.jb : 0;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const bool has = te[t] > tb[t];
+    it.ub[t] = has ? tb[t] - it.jb : 0;
+    it.ue[t] = has ? te[t] - it.jb : 0;
+  }
   return true;
 }
 
@@ -194,7 +214,7 @@ __device__ __forceinline__ int item_of_round(int r) {
   return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SOFTCAP>
+template <int D, bool BF16, bool MASK, bool SOFTCAP>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = PrefillCfg<D>;
@@ -247,7 +267,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         const int item = item_of_round(r);
         if (item >= p.num_items) break;
         PrefillItem it;
-        if (!decode_item<C::BM, C::BN, CAUSAL>(p, item, it) || it.nmax == 0) continue;
+        if (!decode_item<C::BM, C::BN, MASK>(p, item, it) || it.cnt == 0) continue;
         // The previous item's S MMAs must be done with the Q buffer.
         if (qn > 0 && !(ok = w.wait(&sm.q_empty, (qn - 1) & 1, kErrPrefillQ))) break;
         mbar_arrive_expect_tx(&sm.q_full, 2 * C::TILE_BYTES);
@@ -258,7 +278,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
             tma_load_4d(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full, c * 64,
                         it.rq0 + it.m0 + t * C::BM, it.h, it.bcoord);
         ++qn;
-        for (int j = 0; j < it.nmax; ++j, ++g) {
+        for (int j = 0; j < it.cnt; ++j, ++g) {
           const int s = g % C::NS;
           const uint32_t ph = (g / C::NS) & 1;
           if (!(ok = w.wait(&sm.k_empty[s], ph ^ 1, kErrPrefillKEmpty))) break;
@@ -266,14 +286,14 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c)
             tma_load_4d(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s], c * 64,
-                        it.rk0 + j * C::BN, it.hk, it.bcoord);
+                        it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
           ++k_armed;
           if (!(ok = w.wait(&sm.v_empty[s], ph ^ 1, kErrPrefillVEmpty))) break;
           mbar_arrive_expect_tx(&sm.v_full[s], C::TILE_BYTES);
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c)
             tma_load_4d(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s], c * 64,
-                        it.rk0 + j * C::BN, it.hk, it.bcoord);
+                        it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
           ++v_armed;
         }
       }
@@ -320,56 +340,52 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         const int item = item_of_round(r);
         if (item >= p.num_items) break;
         PrefillItem it;
-        if (!decode_item<C::BM, C::BN, CAUSAL>(p, item, it) || it.nmax == 0) continue;
+        if (!decode_item<C::BM, C::BN, MASK>(p, item, it) || it.cnt == 0) continue;
         ok = w.wait(&sm.q_full, qn & 1, kErrPrefillQ) &&
              w.wait(&sm.k_full[g % C::NS], (g / C::NS) & 1, kErrPrefillKFull);
         ++qn;
         if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (it.n[t] > 0) issue_s(t, g);
+          if (it.ub[t] == 0 && it.ue[t] > 0) issue_s(t, g);
         umma_commit(&sm.k_empty[g % C::NS]);
         // Q is free for the next item once the item's last S MMA completes:
         // commit right after that issue so the next Q load overlaps the tail.
-        if (it.nmax == 1) umma_commit(&sm.q_empty);
-        for (int j = 0; ok && j < it.nmax; ++j) {
-          const int gj = g + j;
-          const int s = gj % C::NS;
-          bool v_ready = false, kn_ready = false;
+        if (it.cnt == 1) umma_commit(&sm.q_empty);
+        // Every streamed K/V tile is waited for and released at its step, used
+        // or not (a narrow window can leave a tile to neither query tile).
+        for (int u = 0; ok && u < it.cnt; ++u) {
+          const int gu = g + u;
+          const int s = gu % C::NS;
+          if (!(ok = w.wait(&sm.v_full[s], (gu / C::NS) & 1, kErrPrefillVFull))) break;
+          const bool next = u + 1 < it.cnt;
+          if (next && !(ok = w.wait(&sm.k_full[(gu + 1) % C::NS], ((gu + 1) / C::NS) & 1,
+                                    kErrPrefillKFull)))
+            break;
           for (int t = 0; t < 2; ++t) {
-            if (j >= it.n[t]) continue;
-            if (!v_ready) {
-              if (!(ok = w.wait(&sm.v_full[s], (gj / C::NS) & 1, kErrPrefillVFull))) break;
-              v_ready = true;
+            if (it.ub[t] <= u && u < it.ue[t]) {
+              if (!(ok = w.wait(&sm.p_full[t], pc[t] & 1, kErrPrefillPFull))) break;
+              ++pc[t];
+              // O_t is free once the previous item's epilogue has read it.
+              if (u == it.ub[t] && oc[t] > 0 &&
+                  !(ok = w.wait(&sm.o_free[t], (oc[t] - 1) & 1, kErrPrefillOFinal)))
+                break;
+              tc_fence_after();
+              issue_pv(t, gu, u > it.ub[t]);
+              if (u + 1 == it.ue[t]) umma_commit(&sm.o_final[t]);
             }
-            if (!(ok = w.wait(&sm.p_full[t], pc[t] & 1, kErrPrefillPFull))) break;
-            ++pc[t];
-            // O_t is free once the previous item's epilogue has read it.
-            if (j == 0 && oc[t] > 0 &&
-                !(ok = w.wait(&sm.o_free[t], (oc[t] - 1) & 1, kErrPrefillOFinal)))
-              break;
-            tc_fence_after();
-            issue_pv(t, gj, j > 0);
-            if (j + 1 < it.n[t]) {
-              if (!kn_ready) {
-                const int gn = gj + 1;
-                if (!(ok = w.wait(&sm.k_full[gn % C::NS], (gn / C::NS) & 1, kErrPrefillKFull)))
-                  break;
-                tc_fence_after();
-                kn_ready = true;
-              }
-              issue_s(t, gj + 1);
-            } else {
-              umma_commit(&sm.o_final[t]);
+            if (next && it.ub[t] <= u + 1 && u + 1 < it.ue[t]) {
+              tc_fence_after();
+              issue_s(t, gu + 1);
             }
           }
-          if (v_ready) umma_commit(&sm.v_empty[s]);
-          if (kn_ready) umma_commit(&sm.k_empty[(gj + 1) % C::NS]);
-          if (j == it.nmax - 2) umma_commit(&sm.q_empty);  // last S MMA issued
+          umma_commit(&sm.v_empty[s]);
+          if (next) umma_commit(&sm.k_empty[(gu + 1) % C::NS]);
+          if (u == it.cnt - 2) umma_commit(&sm.q_empty);  // last S MMA issued
         }
         for (int t = 0; t < 2; ++t)
-          if (it.n[t] > 0) ++oc[t];
-        g += it.nmax;
+          if (it.ue[t] > it.ub[t]) ++oc[t];
+        g += it.cnt;
       }
       // All MMAs this thread issued must finish before tensor memory is freed.
       umma_commit(&sm.teardown);
@@ -392,12 +408,13 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       const int item = item_of_round(rr);
       if (item >= p.num_items) break;
       PrefillItem it;
-      if (!decode_item<C::BM, C::BN, CAUSAL>(p, item, it)) continue;
+      if (!decode_item<C::BM, C::BN, MASK>(p, item, it)) continue;
       const int mt = it.m0 + t * C::BM;
       if (mt >= it.Lq) continue;  // this tile has no row
       const int qi = mt + r;      // query index within the sequence
-      const int nt = it.n[t];
-      const int diag = it.Lk - it.Lq;  // bottom-right alignment offset
+      const int nt = it.ue[t] - it.ub[t];  // K/V steps of this tile
+      const int diag = it.Lk - it.Lq;      // bottom-right alignment offset
+      const int last = min(mt + C::BM - 1, it.Lq - 1);
 
       float m_use = -INFINITY;  // exp2 subtrahend currently in use (log2 units)
       float l = 0.0f;           // running denominator w.r.t. m_use
@@ -428,12 +445,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           tanh128(s, p.scale * p.softcap_inv);
           a_coef = p.softcap * kLog2e;
         }
-        const int j0 = j * C::BN;
-        if ((j0 + C::BN > it.Lk) || (CAUSAL && (j0 + C::BN - 1 > mt + diag))) {
-          int lim = it.Lk - 1 - j0;
-          if (CAUSAL) lim = min(lim, qi + diag - j0);
+        const int j0 = (it.jb + it.ub[t] + j) * C::BN;  // first key of this K/V tile
+        if ((j0 + C::BN > it.Lk) ||
+            (MASK && p.win_right >= 0 && j0 + C::BN - 1 > mt + diag + p.win_right) ||
+            (MASK && p.win_left >= 0 && j0 < last + diag - p.win_left)) {
+          int hi = it.Lk - 1 - j0, lo = 0;  // kept columns [lo, hi] of this row
+          if (MASK && p.win_right >= 0) hi = min(hi, qi + diag + p.win_right - j0);
+          if (MASK && p.win_left >= 0) lo = qi + diag - p.win_left - j0;
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+          for (int c = 0; c < 128; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : -INFINITY;
         }
         const float m_new = fmaxf(m_use, max128(s) * a_coef);  // a_coef > 0: order kept
         float alpha = 1.0f;
@@ -547,10 +567,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SOFTCAP>
+template <int D, bool BF16, bool MASK, bool SOFTCAP>
 static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream_t stream) {
   using C = PrefillCfg<D>;
-  auto kern = attn_prefill_kernel<D, BF16, CAUSAL, SOFTCAP>;
+  auto kern = attn_prefill_kernel<D, BF16, MASK, SOFTCAP>;
   const int smem = static_cast<int>(sizeof(PrefillSmem<C>)) + 1024;
   static bool configured = false;  // per instantiation; attribute set is idempotent
   if (!configured) {
@@ -562,12 +582,15 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool causal,
+cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool masked,
                            bool softcap, cudaStream_t stream, char* name, size_t name_len) {
+  const char* mask = !masked ? "nomask"
+                     : (p.win_left < 0 && p.win_right == 0) ? "causal"
+                                                            : "window";
   snprintf(name, name_len, "attn_prefill_tcgen05_d%d_%s_%s_%s_m256n128_persistent", d,
-           bf16 ? "bf16" : "f16", causal ? "causal" : "nomask", softcap ? "softcap" : "nocap");
+           bf16 ? "bf16" : "f16", mask, softcap ? "softcap" : "nocap");
 #define ATTN_PREFILL_CASE(D_, B_, C_, S_)                                        \
-  if (d == D_ && bf16 == B_ && causal == C_ && softcap == S_)                    \
+  if (d == D_ && bf16 == B_ && masked == C_ && softcap == S_)                    \
     return launch_prefill_t<D_, B_, C_, S_>(p, grid, stream);
   ATTN_PREFILL_CASE(64, true, false, false)
   ATTN_PREFILL_CASE(64, true, false, true)

@@ -67,11 +67,24 @@ typedef struct {
   int64_t row;
 } attn_strides;
 
+/*
+ * Options.  A zero-initialised struct is plain softmax attention with the
+ * default scale.  Masks (Composable Kernel mask from window_size_left /
+ * window_size_right, generic attention mask) are bottom-right aligned: query
+ * row i of a sequence with Lq queries and Lk keys sits on key diagonal
+ * i + Lk - Lq.  Causal keeps keys j <= i + Lk - Lq.  A window keeps
+ * i + Lk - Lq - window_left <= j <= i + Lk - Lq + window_right, a negative
+ * bound meaning unbounded on that side; with causal also set both apply.
+ * A row that keeps no key (and has no sink) gives O = 0, LSE = -inf.
+ */
 typedef struct {
   float scale;       /* softmax scale; <= 0 selects 1/sqrt(d) (DefTruth FA2 kernel prologue) */
   int causal;        /* nonzero: bottom-right aligned causal mask */
   float softcap;     /* > 0: s <- softcap * tanh(s / softcap); <= 0: off */
   const float* sink; /* device fp32 [Hq] sink logits (natural-log units), or NULL */
+  int use_window;    /* nonzero: apply window_left / window_right */
+  int window_left;   /* keys kept left of the diagonal (< 0: all) */
+  int window_right;  /* keys kept right of the diagonal (< 0: all) */
 } attn_opts;
 
 /*
@@ -118,8 +131,12 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
  *   multiple of 16 and <= 256.
  *   num_splits: 0 = choose automatically (attn_paged_auto_splits), else
  *   1..64.  Split s of sequence b covers logical pages
- *   [s*c, min((s+1)*c, ceil(L_b/page_size))), c = ceil(max_pages_per_seq /
- *   num_splits); a split with no page is empty (O = 0, LSE = -inf).
+ *   [f_b + s*c, min(f_b + (s+1)*c, e_b)), c = ceil(W / num_splits); a split
+ *   with no page is empty (O = 0, LSE = -inf).  Without a window f_b = 0,
+ *   e_b = ceil(L_b/page_size) and W = max_pages_per_seq.  With a window the
+ *   pages are those holding a key some query row keeps: f_b = floor(k_lo /
+ *   page_size), e_b = ceil(k_hi / page_size) for the kept key range
+ *   [k_lo, k_hi) of the sequence, and W = attn_paged_window_pages().
  *   When num_splits > 1, o_partial (fp32 [num_splits][B][Hq][Lq][d]) and
  *   lse_partial (fp32 [num_splits][B][Hq][Lq]) are caller-owned scratch of
  *   attn_paged_workspace_bytes() bytes in total, and attn_splitkv_combine is
@@ -179,8 +196,17 @@ attn_status attn_splitkv_combine(const float* o_partial, const float* lse_partia
 /* Bytes of split-KV scratch attn_fwd_paged needs (o_partial then lse_partial). */
 size_t attn_paged_workspace_bytes(int B, int Lq, int Hq, int d, int num_splits);
 
-/* The split count attn_fwd_paged uses for num_splits = 0 on the current device. */
+/* The split count attn_fwd_paged uses for num_splits = 0 on the current device
+ * (pass W of attn_paged_window_pages as max_pages_per_seq). */
 int attn_paged_auto_splits(int B, int Hkv, int max_pages_per_seq);
+
+/* W of the paged split layout: the most logical pages of one sequence that
+ * hold a key some query row keeps.  max_pages_per_seq without a left window,
+ * else min(max_pages_per_seq, ceil((Lq + window_left) / page_size) + 1)
+ * (the kept keys of a sequence of length L are [max(0, L - Lq - window_left),
+ * L), as every row's right bound reaches the last key or beyond).
+ * opts may be NULL. */
+int attn_paged_window_pages(int Lq, int page_size, int max_pages_per_seq, const attn_opts* opts);
 
 /* Human-readable name of a status. */
 const char* attn_status_string(attn_status status);

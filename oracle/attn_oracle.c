@@ -264,9 +264,12 @@ int oracle_attn_paged(const double* q, const double* k_pool, const double* v_poo
 }
 
 /* Split-KV partials of the paged problem.  Split s of sequence b covers the
- * key pages [s*chunk_pages, min((s+1)*chunk_pages, pages_b)), pages_b =
+ * key pages [f + s*chunk_pages, min(f + (s+1)*chunk_pages, pages_b)), pages_b =
  * ceil(seqlens_k[b] / page); a split with no key page is empty (O = 0,
- * LSE = -inf).  No sink in a split (the merge adds it once).
+ * LSE = -inf).  No sink in a split (the merge adds it once).  f = 0 without a
+ * left window; with one, f is the page of the first key any query row keeps,
+ * max(0, L - Lq - wl) (every row's right bound is at or past the last key),
+ * so the splits tile only the pages the window reaches. 
  * o_part [S][B][Hq][Lq][d], lse_part [S][B][Hq][Lq]. */
 int oracle_attn_paged_partials(const double* q, const double* k_pool, const double* v_pool,
                                const int32_t* block_table, const int32_t* seqlens_k,
@@ -291,9 +294,11 @@ int oracle_attn_paged_partials(const double* q, const double* k_pool, const doub
         double* s_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
         double* p_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
         unsigned char* keep = (unsigned char*)malloc(Lk > 0 ? Lk : 1);
+        long first = 0;
+        if (wl >= 0 && (long)Lk - Lq - wl > 0) first = ((long)Lk - Lq - wl) / page;
         for (int s = 0; s < num_splits; ++s) {
-            long j0 = (long)s * chunk_pages * page;
-            long j1 = (long)(s + 1) * chunk_pages * page;
+            long j0 = (first + (long)s * chunk_pages) * page;
+            long j1 = (first + (long)(s + 1) * chunk_pages) * page;
             if (j1 > Lk) j1 = Lk;
             for (int i = 0; i < Lq; ++i) {
                 long ridx = ((long)b * Hq + h) * Lq + i;

@@ -97,6 +97,26 @@ def test_workspace_and_auto_splits():
     assert A.attn_paged_auto_splits(1, 1, 1) == 1
 
 
+def test_paged_window_pages():
+    """W of the paged split layout: every page without a left window, else the
+    pages the band [L - Lq - left, L) can touch (its length over the page size,
+    plus one for a band that starts inside a page), capped by the table."""
+    W = A.attn_paged_window_pages
+    assert W(1, 64, 100) == 100                                  # no window
+    assert W(1, 64, 100, window=(-1, 5)) == 100                  # right bound only
+    assert W(1, 64, 100, causal=True) == 100
+    assert W(1, 64, 100, window=(255, -1)) == 4 + 1              # 256 keys: 4 pages + 1
+    assert W(1, 64, 100, window=(256, -1)) == 5 + 1
+    assert W(4, 16, 100, window=(0, 0)) == 1 + 1
+    assert W(1, 64, 3, window=(1000, -1)) == 3                   # capped by the table
+    # The band [L - Lq - left, L) never spans more pages than W, wherever it starts.
+    for Lq, page, left in ((1, 64, 300), (4, 32, 40), (2, 16, 0)):
+        w = W(Lq, page, 1000, window=(left, -1))
+        for L in range(Lq + left, Lq + left + 3 * page):
+            lo = L - Lq - left
+            assert (L + page - 1) // page - lo // page <= w
+
+
 def test_combine_validation():
     lib = A.library()
     p = 1 << 12

@@ -268,22 +268,26 @@ def pin_paged_equals_contiguous(mutant=0):
 
 def pin_splits_combine_to_unsplit(mutant=0):
     """Split-KV partials merged by the combine equal the unsplit result (1e-12),
-    including empty splits, the sink added once in the merge, and causal Lq > 1."""
+    including empty splits, the sink added once in the merge, causal Lq > 1 and
+    window bands (splits laid from the band's first page)."""
     r = _rng(12)
     page = 4
     q, kp, vp, bt, lens = _paged_case(r, page=page, lens=(9, 4, 1))
     sink = r.standard_normal(4)
-    for causal in (False, True):
+    # With a left window the splits start at the page of the first kept key;
+    # every layout below spans at least the pages the band can reach.
+    for causal, window in ((False, (-1, -1)), (True, (-1, -1)), (True, (2, -1)),
+                           (False, (1, 1)), (False, (5, 0))):
         for num_splits, chunk in ((1, 3), (2, 2), (4, 1), (3, 2)):
             op, lp = oracle.attn_paged_partials(q, kp, vp, bt, lens, num_splits, chunk, 0.4,
-                                                causal, mutant=mutant)
+                                                causal, mutant=mutant, window=window)
             B, Lq, Hq, d = q.shape
             rows = B * Hq * Lq
             sink_rows = np.broadcast_to(sink[None, :, None], (B, Hq, Lq)).reshape(-1)
             o, lse = oracle.combine(op.reshape(num_splits, rows, d), lp.reshape(num_splits, rows),
                                     sink_rows, mutant=mutant)
             o_ref, l_ref = oracle.attn_paged(q, kp, vp, bt, lens, 0.4, causal, sink=sink,
-                                             mutant=mutant)
+                                             mutant=mutant, window=window)
             _close(o.reshape(B, Hq, Lq, d), o_ref.transpose(0, 2, 1, 3), 1e-12, "combine O")
             _close(lse.reshape(B, Hq, Lq), l_ref, 1e-12, "combine LSE")
 
