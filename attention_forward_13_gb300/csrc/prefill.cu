@@ -70,6 +70,9 @@ struct PrefillSmem {
   uint64_t teardown;
   uint32_t tmem_base;
   int abort_flag;
+  // Epilogue staging, one 32-row x 128-byte block per softmax warp: rows go
+  // in from the thread that owns them and out as whole 128-byte lines.
+  alignas(128) uint4 ostage[8][32 * 8];
 };
 
 // Maximum of 128 values: a tree of 3-input max instructions (64 instructions,
@@ -525,17 +528,24 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         const float lse = (ltot > 0.0f) ? (mfin + __log2f(ltot)) * kLn2 : -INFINITY;
         p.lse[it.b * p.lse_batch + it.h * p.lse_head + it.rq0 + qi] = lse;
       }
-      T* orow = reinterpret_cast<T*>(p.o) + it.b * p.o_batch + it.h * p.o_head +
-                static_cast<int64_t>(it.rq0 + qi) * p.o_row;
-      uint4* dst = reinterpret_cast<uint4*>(orow);
+      T* obase = reinterpret_cast<T*>(p.o) + it.b * p.o_batch + it.h * p.o_head +
+                 static_cast<int64_t>(it.rq0 + mt + (warp & 3) * 32) * p.o_row;
+      const int rows_left = it.Lq - (mt + (warp & 3) * 32);  // valid rows of this warp
       if (have_o) {
+        // 64 columns per round: each thread packs its row into the stage
+        // (16-byte pieces, XOR-swizzled by row so a warp's stores hit distinct
+        // banks), then the warp writes 4 rows x 128 contiguous bytes per
+        // instruction instead of 32 scattered 16-byte pieces.
+        uint4* stage = sm.ostage[warp & 7];
+        const int lr = lane & 31;
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tmem_ld32(tO + c, ov);
-          tmem_ld_wait();
-          reg_fence(ov);
-          if (row_ok) {
+        for (int c0 = 0; c0 < D; c0 += 64) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c0 + 32 * h, ov);
+            tmem_ld_wait();
+            reg_fence(ov);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               uint32_t w4[4];
@@ -545,14 +555,27 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
                 const float bb = __uint_as_float(ov[8 * q4 + 2 * i + 1]) * oscale;
                 w4[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
               }
-              dst[c / 8 + q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              stage[lr * 8 + ((4 * h + q4) ^ (lr & 7))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
           }
+          if (c0 + 64 == D) {
+            // O_t has been read: the next item's first P.V may overwrite it.
+            tc_fence_before();
+            mbar_arrive(&sm.o_free[t]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + (lr >> 3), q = lr & 7;
+            const uint4 v4 = stage[rr * 8 + (q ^ (rr & 7))];
+            if (rr < rows_left)
+              *reinterpret_cast<uint4*>(obase + static_cast<int64_t>(rr) * p.o_row + c0 + 8 * q) =
+                  v4;
+          }
+          __syncwarp();
         }
-        // O_t may now be overwritten by the next item's first P.V.
-        tc_fence_before();
-        mbar_arrive(&sm.o_free[t]);
       } else if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(obase + static_cast<int64_t>(r & 31) * p.o_row);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
       }
