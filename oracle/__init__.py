@@ -56,14 +56,15 @@ def _lib(mutant: int = 0) -> ctypes.CDLL:
         if mutant not in _libs:
             lib = ctypes.CDLL(build(mutant))
             m = [ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double]
+            x = [ctypes.c_int, _D]  # top_left, alibi slopes [B][Hq]
             lib.oracle_attn_dense.argtypes = [_D, _D, _D, _D, _D] + [ctypes.c_int] * 6 + m + [
-                _D, _D, _D]
+                _D, _D, _D] + x + [_D]
             lib.oracle_attn_varlen.argtypes = [_D, _D, _D, _D, _D, _I, _I] + [ctypes.c_int] * 4 + m + [
-                _D]
+                _D] + x
             lib.oracle_attn_paged.argtypes = [_D, _D, _D, _I, _I, _D, _D] + [ctypes.c_int] * 7 + m + [
-                _D]
+                _D] + x
             lib.oracle_attn_paged_partials.argtypes = [_D, _D, _D, _I, _I, _D, _D] + [
-                ctypes.c_int] * 9 + m
+                ctypes.c_int] * 9 + m + x
             lib.oracle_combine.argtypes = [_D, _D, ctypes.c_int, ctypes.c_long, ctypes.c_int, _D,
                                            _D, _D]
             lib.oracle_mutant_id.restype = ctypes.c_int
@@ -87,15 +88,23 @@ def _p(a):
     return a.ctypes.data_as(_I)
 
 
+def _alibi(alibi, B, Hq):
+    """ALiBi slopes broadcast to [B][Hq] (a [Hq] vector is shared by all batches)."""
+    if alibi is None:
+        return None
+    return _f64(np.broadcast_to(np.asarray(alibi, dtype=np.float64), (B, Hq)))
+
+
 def _check(rc: int, fn: str):
     if rc != 0:
         raise ValueError(f"oracle {fn}: invalid arguments")
 
 
 def attn_dense(q, k, v, scale, causal=False, softcap=0.0, sink=None, want_sp=False, mutant=0,
-               window=(-1, -1)):
+               window=(-1, -1), top_left=False, alibi=None, bias=None):
     """Dense attention.  q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] -> (o [B,Hq,Lq,d], lse [B,Hq,Lq])
-    and, if ``want_sp``, the materialised S and P [B,Hq,Lq,Lk]."""
+    and, if ``want_sp``, the materialised S and P [B,Hq,Lq,Lk].  ``alibi``: slopes
+    [B,Hq] or [Hq]; ``bias``: additive bias broadcastable to [B,Hq,Lq,Lk]."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Lq, d = q.shape
     _, Hkv, Lk, _ = k.shape
@@ -104,10 +113,13 @@ def attn_dense(q, k, v, scale, causal=False, softcap=0.0, sink=None, want_sp=Fal
     sk = _f64(sink) if sink is not None else None
     s_out = np.zeros((B, Hq, Lq, Lk)) if want_sp else None
     p_out = np.zeros((B, Hq, Lq, Lk)) if want_sp else None
+    al = _alibi(alibi, B, Hq)
+    bi = None if bias is None else _f64(np.broadcast_to(np.asarray(bias, np.float64),
+                                                        (B, Hq, Lq, Lk)))
     rc = _lib(mutant).oracle_attn_dense(_p(q), _p(k), _p(v), _p(o), _p(lse), B, Hq, Hkv, Lq, Lk,
                                         d, float(scale), int(bool(causal)), int(window[0]),
                                         int(window[1]), float(softcap), _p(sk), _p(s_out),
-                                        _p(p_out))
+                                        _p(p_out), int(bool(top_left)), _p(al), _p(bi))
     _check(rc, "attn_dense")
     if want_sp:
         return o, lse, s_out, p_out
@@ -115,7 +127,7 @@ def attn_dense(q, k, v, scale, causal=False, softcap=0.0, sink=None, want_sp=Fal
 
 
 def attn_varlen(q, k, v, cu_q, cu_k, scale, causal=False, softcap=0.0, sink=None, mutant=0,
-                window=(-1, -1)):
+                window=(-1, -1), top_left=False, alibi=None):
     """Varlen attention.  q [total_q,Hq,d], k/v [total_k,Hkv,d], cu int32 [B+1]
     -> (o [total_q,Hq,d], lse [Hq,total_q])."""
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -128,13 +140,14 @@ def attn_varlen(q, k, v, cu_q, cu_k, scale, causal=False, softcap=0.0, sink=None
     sk = _f64(sink) if sink is not None else None
     rc = _lib(mutant).oracle_attn_varlen(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(cu_q), _p(cu_k),
                                          B, Hq, Hkv, d, float(scale), int(bool(causal)),
-                                         int(window[0]), int(window[1]), float(softcap), _p(sk))
+                                         int(window[0]), int(window[1]), float(softcap), _p(sk),
+                                         int(bool(top_left)), _p(_alibi(alibi, B, Hq)))
     _check(rc, "attn_varlen")
     return o, lse
 
 
 def attn_paged(q, k_pool, v_pool, block_table, seqlens_k, scale, causal=False, softcap=0.0,
-               sink=None, mutant=0, window=(-1, -1)):
+               sink=None, mutant=0, window=(-1, -1), top_left=False, alibi=None):
     """Paged-KV attention.  q [B,Lq,Hq,d], pools [P,page,Hkv,d], block_table int32
     [B,max_pages], seqlens_k int32 [B] -> (o [B,Lq,Hq,d], lse [B,Hq,Lq])."""
     q, kp, vp = _f64(q), _f64(k_pool), _f64(v_pool)
@@ -147,13 +160,15 @@ def attn_paged(q, k_pool, v_pool, block_table, seqlens_k, scale, causal=False, s
     rc = _lib(mutant).oracle_attn_paged(_p(q), _p(kp), _p(vp), _p(bt), _p(sl), _p(o), _p(lse),
                                         B, Lq, Hq, Hkv, d, page, bt.shape[1], float(scale),
                                         int(bool(causal)), int(window[0]), int(window[1]),
-                                        float(softcap), _p(sk))
+                                        float(softcap), _p(sk), int(bool(top_left)),
+                                        _p(_alibi(alibi, B, Hq)))
     _check(rc, "attn_paged")
     return o, lse
 
 
 def attn_paged_partials(q, k_pool, v_pool, block_table, seqlens_k, num_splits, chunk_pages,
-                        scale, causal=False, softcap=0.0, mutant=0, window=(-1, -1)):
+                        scale, causal=False, softcap=0.0, mutant=0, window=(-1, -1),
+                        top_left=False, alibi=None):
     """Split-KV partials of the paged problem -> (o_part [S,B,Hq,Lq,d], lse_part [S,B,Hq,Lq])."""
     q, kp, vp = _f64(q), _f64(k_pool), _f64(v_pool)
     bt, sl = _i32(block_table), _i32(seqlens_k)
@@ -164,7 +179,8 @@ def attn_paged_partials(q, k_pool, v_pool, block_table, seqlens_k, num_splits, c
     rc = _lib(mutant).oracle_attn_paged_partials(
         _p(q), _p(kp), _p(vp), _p(bt), _p(sl), _p(o), _p(lse), B, Lq, Hq, Hkv, d, page,
         bt.shape[1], int(num_splits), int(chunk_pages), float(scale), int(bool(causal)),
-        int(window[0]), int(window[1]), float(softcap))
+        int(window[0]), int(window[1]), float(softcap), int(bool(top_left)),
+        _p(_alibi(alibi, B, Hq)))
     _check(rc, "attn_paged_partials")
     return o, lse
 
@@ -185,4 +201,4 @@ def mutant_id(mutant: int) -> int:
     return _lib(mutant).oracle_mutant_id()
 
 
-MUTANTS = tuple(range(1, 10))
+MUTANTS = tuple(range(1, 12))

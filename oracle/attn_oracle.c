@@ -12,7 +12,7 @@
  *   Composable Kernel, fmha_fwd_pagedkv_kernel.hpp, header comment:
  *     S   = Q . K^T                       (per head, fp64 here)
  *     S'  = S * scale
- *     S'' = S' (+ bias: not in scope)
+ *     S'' = S' + Bias                  (elementwise bias, [Lq][Lk] per head)
  *     P   = softmax(S'')   row by row
  *     O   = P . V
  *   DefTruth flash_attn_mma_share_kv_F32F16F16F32.cu, kernel prologue:
@@ -32,6 +32,18 @@
  *     kargs, same bottom-right alignment) keeps j iff
  *       i + (Lk - Lq) - left <= j <= i + (Lk - Lq) + right,
  *     a negative size meaning unbounded on that side; causal is right = 0.
+ *     MASK_FROM_TOP_LEFT instead puts query i on key diagonal i (no Lk - Lq
+ *     shift), for both the causal and the window bounds.
+ *   Composable Kernel, operator() (position encoding, ALiBi): one slope per
+ *     (batch, query head) (alibi_slope_ptr + i_batch * stride + i_nhead), the
+ *     bias aligned like the mask (bottom-right unless MASK_FROM_TOP_LEFT).  The
+ *     position term itself is not printed on the page; the reading used is the
+ *     ALiBi definition  S'' = S' - slope * |diag(i) - j|,  diag(i) the key on
+ *     query i's diagonal, added to the scaled (natural-log) score.
+ *   Composable Kernel, FmhaFwdCommonBiasKargs (bias_ptr with row, head and
+ *     batch strides): the elementwise bias is added to the scaled score.  With
+ *     the soft-cap the order is not on the pages; those combinations are not
+ *     evaluated (the library rejects them).
  *   FlashAttention-3 hopper/epilogue_fwd.hpp, CollectiveEpilogueFwd::store_zero:
  *     a row with no key to attend to gets O = 0 and LSE = -inf (with a sink:
  *     O = 0 and LSE = sigma).
@@ -75,14 +87,18 @@
 
 /* One query row against Lk keys of one head.
  *   q: [d], k: rows kbase + j*kstride (j < Lk), v likewise.
- *   qi: query index, used only by the causal rule.
+ *   diag: index (into these Lk keys) of the key on this row's diagonal; the
+ *     causal, window and ALiBi terms are measured from it.
+ *   bias_row: [Lk] additive bias of this row, or NULL.
+ *   alibi: ALiBi slope of this row's (batch, head) (0: none).
  *   s_row/p_row: scratch of length Lk (also returned to the caller when asked).
  *   keep: scratch of length Lk.
  *   o: [d] output row; *lse: output.
  * Returns nothing; empty rows follow the store_zero convention. */
 static void row_forward(const double* q, const double* k, const double* v, long kvstride,
-                        int Lq, int Lk, int qi, int d, double scale, int causal, int wl, int wr,
-                        double softcap, int has_sink, double sink,
+                        int Lk, long diag, int d, double scale, int causal, int wl, int wr,
+                        double softcap, const double* bias_row, double alibi,
+                        int has_sink, double sink,
                         double* s_row, double* p_row, unsigned char* keep,
                         double* o, double* lse)
 {
@@ -99,12 +115,13 @@ static void row_forward(const double* q, const double* k, const double* v, long 
             if (MUTANT(3)) s = tanh(s / softcap);          /* dropped outer cap */
             else s = softcap * tanh(s / softcap);
         }
+        if (bias_row) s += bias_row[j];
+        if (alibi != 0.0) {
+            const double dist = fabs((double)(diag - (long)j));
+            s += MUTANT(10) ? alibi * dist : -alibi * dist; /* MUTANT 10: sign flipped */
+        }
         s_row[j] = s;
-        /* bottom-right alignment of the causal and window bounds */
-        const long diag = (long)qi + (long)(Lk - Lq);
-        long lim = diag;
-        if (MUTANT(4)) lim = qi;                           /* top-left instead */
-        int kept = !causal || (long)j <= lim;
+        int kept = !causal || (long)j <= diag;
         if (wr >= 0 && (long)j > diag + wr) kept = 0;
         if (wl >= 0 && (long)j < diag - wl + (MUTANT(9) ? 1 : 0)) kept = 0; /* MUTANT 9: off by one */
         keep[j] = (unsigned char)kept;
@@ -146,6 +163,13 @@ static void row_forward(const double* q, const double* k, const double* v, long 
     }
 }
 
+/* Key on query i's diagonal: bottom-right (i + Lk - Lq) unless top-left. */
+static long row_diag(int i, int Lq, int Lk, int top_left)
+{
+    if (top_left || MUTANT(4)) return i;  /* MUTANT 4: top-left instead of bottom-right */
+    return (long)i + (long)(Lk - Lq);
+}
+
 static int kv_head_of(int h, int Hq, int Hkv)
 {
     int g = Hq / Hkv;
@@ -153,12 +177,14 @@ static int kv_head_of(int h, int Hq, int Hkv)
     return h / g;
 }
 
-/* Dense [B,H,L,d].  s_out/p_out: optional [B][Hq][Lq][Lk]. */
+/* Dense [B,H,L,d].  s_out/p_out: optional [B][Hq][Lq][Lk].
+ * alibi: optional slopes [B][Hq]; bias: optional [B][Hq][Lq][Lk]. */
 int oracle_attn_dense(const double* q, const double* k, const double* v,
                       double* o, double* lse,
                       int B, int Hq, int Hkv, int Lq, int Lk, int d,
                       double scale, int causal, int wl, int wr, double softcap,
-                      const double* sink, double* s_out, double* p_out)
+                      const double* sink, double* s_out, double* p_out,
+                      int top_left, const double* alibi, const double* bias)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Lq < 0 || Lk < 0 || d <= 0) return 1;
     long nbh = (long)B * Hq;
@@ -173,7 +199,13 @@ int oracle_attn_dense(const double* q, const double* k, const double* v,
         double* p_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
         unsigned char* keep = (unsigned char*)malloc(Lk > 0 ? Lk : 1);
         for (int i = 0; i < Lq; ++i) {
-            row_forward(qh + (long)i * d, kh, vh, d, Lq, Lk, i, d, scale, causal, wl, wr, softcap,
+            const double* brow = NULL;
+            if (bias) {
+                int bi = MUTANT(11) ? (i + 1) % Lq : i;  /* MUTANT 11: bias row shifted */
+                brow = bias + (((long)b * Hq + h) * Lq + bi) * Lk;
+            }
+            row_forward(qh + (long)i * d, kh, vh, d, Lk, row_diag(i, Lq, Lk, top_left), d, scale,
+                        causal, wl, wr, softcap, brow, alibi ? alibi[(long)b * Hq + h] : 0.0,
                         sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
                         o + (((long)b * Hq + h) * Lq + i) * d,
                         lse + ((long)b * Hq + h) * Lq + i);
@@ -191,7 +223,7 @@ int oracle_attn_varlen(const double* q, const double* k, const double* v,
                        const int32_t* cu_q, const int32_t* cu_k,
                        int B, int Hq, int Hkv, int d,
                        double scale, int causal, int wl, int wr, double softcap,
-                       const double* sink)
+                       const double* sink, int top_left, const double* alibi)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0) return 1;
     int total_q = cu_q[B];
@@ -210,8 +242,10 @@ int oracle_attn_varlen(const double* q, const double* k, const double* v,
         const double* vh = v + (long)k0 * kvstride + (long)hk * d;
         for (int i = 0; i < Lq; ++i) {
             long row = q0 + i;
-            row_forward(q + (row * Hq + h) * d, kh, vh, kvstride, Lq, Lk, i, d, scale, causal, wl,
-                        wr, softcap, sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
+            row_forward(q + (row * Hq + h) * d, kh, vh, kvstride, Lk, row_diag(i, Lq, Lk, top_left),
+                        d, scale, causal, wl, wr, softcap, NULL,
+                        alibi ? alibi[(long)b * Hq + h] : 0.0,
+                        sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
                         o + (row * Hq + h) * d, lse + (long)h * total_q + row);
         }
         free(s_row); free(p_row); free(keep);
@@ -237,7 +271,7 @@ int oracle_attn_paged(const double* q, const double* k_pool, const double* v_poo
                       double* o, double* lse,
                       int B, int Lq, int Hq, int Hkv, int d, int page, int max_pages,
                       double scale, int causal, int wl, int wr, double softcap,
-                      const double* sink)
+                      const double* sink, int top_left, const double* alibi)
 {
     if (B < 0 || Lq < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || page <= 0) return 1;
     long nbh = (long)B * Hq;
@@ -254,8 +288,10 @@ int oracle_attn_paged(const double* q, const double* k_pool, const double* v_poo
         double* p_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
         unsigned char* keep = (unsigned char*)malloc(Lk > 0 ? Lk : 1);
         for (int i = 0; i < Lq; ++i) {
-            row_forward(q + (((long)b * Lq + i) * Hq + h) * d, kg, vg, d, Lq, Lk, i, d, scale,
-                        causal, wl, wr, softcap, sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
+            row_forward(q + (((long)b * Lq + i) * Hq + h) * d, kg, vg, d, Lk,
+                        row_diag(i, Lq, Lk, top_left), d, scale, causal, wl, wr, softcap, NULL,
+                        alibi ? alibi[(long)b * Hq + h] : 0.0,
+                        sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
                         o + (((long)b * Lq + i) * Hq + h) * d, lse + ((long)b * Hq + h) * Lq + i);
         }
         free(kg); free(vg); free(s_row); free(p_row); free(keep);
@@ -276,7 +312,8 @@ int oracle_attn_paged_partials(const double* q, const double* k_pool, const doub
                                double* o_part, double* lse_part,
                                int B, int Lq, int Hq, int Hkv, int d, int page, int max_pages,
                                int num_splits, int chunk_pages,
-                               double scale, int causal, int wl, int wr, double softcap)
+                               double scale, int causal, int wl, int wr, double softcap,
+                               int top_left, const double* alibi)
 {
     if (B < 0 || Lq < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || page <= 0 ||
         num_splits <= 0 || chunk_pages <= 0) return 1;
@@ -295,7 +332,9 @@ int oracle_attn_paged_partials(const double* q, const double* k_pool, const doub
         double* p_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
         unsigned char* keep = (unsigned char*)malloc(Lk > 0 ? Lk : 1);
         long first = 0;
-        if (wl >= 0 && (long)Lk - Lq - wl > 0) first = ((long)Lk - Lq - wl) / page;
+        /* first key any row keeps: the left bound of row 0 */
+        if (wl >= 0 && row_diag(0, Lq, Lk, top_left) - wl > 0)
+            first = (row_diag(0, Lq, Lk, top_left) - wl) / page;
         for (int s = 0; s < num_splits; ++s) {
             long j0 = (first + (long)s * chunk_pages) * page;
             long j1 = (first + (long)(s + 1) * chunk_pages) * page;
@@ -309,15 +348,12 @@ int oracle_attn_paged_partials(const double* q, const double* k_pool, const doub
                     *lrow = -INFINITY;
                     continue;
                 }
-                /* Scores over the split's keys only; the causal rule uses the
-                 * absolute key index j0 + j, so shift the query index instead. */
+                /* Scores over the split's keys only: the diagonal is measured
+                 * in the split's own key indices (absolute key = j0 + j). */
                 int Lks = (int)(j1 - j0);
-                /* keep iff (j0 + j) <= i + (Lk - Lq)  <=>  j <= i' + (Lks - Lq)
-                 * with i' = i + (Lk - Lks) - j0 */
-                int ishift = (int)(i + (Lk - Lks) - j0);
-                /* row_forward evaluates j <= ishift + (Lks - Lq) */
                 row_forward(q + (((long)b * Lq + i) * Hq + h) * d, kg + j0 * d, vg + j0 * d, d,
-                            Lq, Lks, ishift, d, scale, causal, wl, wr, softcap, 0, 0.0,
+                            Lks, row_diag(i, Lq, Lk, top_left) - j0, d, scale, causal, wl, wr,
+                            softcap, NULL, alibi ? alibi[(long)b * Hq + h] : 0.0, 0, 0.0,
                             s_row, p_row, keep, orow, lrow);
             }
         }

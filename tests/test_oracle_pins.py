@@ -255,13 +255,17 @@ def pin_paged_equals_contiguous(mutant=0):
     r = _rng(11)
     page = 4
     q, kp, vp, bt, lens = _paged_case(r, page=page)
-    for causal in (False, True):
-        o, lse = oracle.attn_paged(q, kp, vp, bt, lens, 0.4, causal, mutant=mutant)
+    slopes = np.abs(r.standard_normal((len(lens), q.shape[2])))
+    for causal, tl, al in ((False, False, None), (True, False, None), (True, True, slopes),
+                           (False, False, slopes)):
+        o, lse = oracle.attn_paged(q, kp, vp, bt, lens, 0.4, causal, mutant=mutant, top_left=tl,
+                                   alibi=al)
         for b in range(len(lens)):
             kc = _contiguous_from_paged(kp, bt, lens, b, page)[None]
             vc = _contiguous_from_paged(vp, bt, lens, b, page)[None]
             qd = q[b].transpose(1, 0, 2)[None]  # [1][Hq][Lq][d]
-            od, ld = oracle.attn_dense(qd, kc, vc, 0.4, causal, mutant=mutant)
+            od, ld = oracle.attn_dense(qd, kc, vc, 0.4, causal, mutant=mutant, top_left=tl,
+                                       alibi=None if al is None else al[b:b + 1])
             _close(o[b].transpose(1, 0, 2), od[0], 0.0, "paged O")
             _close(lse[b], ld[0], 0.0, "paged LSE")
 
@@ -276,18 +280,23 @@ def pin_splits_combine_to_unsplit(mutant=0):
     sink = r.standard_normal(4)
     # With a left window the splits start at the page of the first kept key;
     # every layout below spans at least the pages the band can reach.
-    for causal, window in ((False, (-1, -1)), (True, (-1, -1)), (True, (2, -1)),
-                           (False, (1, 1)), (False, (5, 0))):
+    slopes = np.abs(r.standard_normal((len(lens), 4)))
+    for causal, window, tl, al in ((False, (-1, -1), False, None), (True, (-1, -1), False, None),
+                                   (True, (2, -1), False, None), (False, (1, 1), False, None),
+                                   (False, (5, 0), False, None), (True, (2, -1), True, slopes),
+                                   (False, (-1, -1), False, slopes)):
         for num_splits, chunk in ((1, 3), (2, 2), (4, 1), (3, 2)):
             op, lp = oracle.attn_paged_partials(q, kp, vp, bt, lens, num_splits, chunk, 0.4,
-                                                causal, mutant=mutant, window=window)
+                                                causal, mutant=mutant, window=window,
+                                                top_left=tl, alibi=al)
             B, Lq, Hq, d = q.shape
             rows = B * Hq * Lq
             sink_rows = np.broadcast_to(sink[None, :, None], (B, Hq, Lq)).reshape(-1)
             o, lse = oracle.combine(op.reshape(num_splits, rows, d), lp.reshape(num_splits, rows),
                                     sink_rows, mutant=mutant)
             o_ref, l_ref = oracle.attn_paged(q, kp, vp, bt, lens, 0.4, causal, sink=sink,
-                                             mutant=mutant, window=window)
+                                             mutant=mutant, window=window, top_left=tl,
+                                             alibi=al)
             _close(o.reshape(B, Hq, Lq, d), o_ref.transpose(0, 2, 1, 3), 1e-12, "combine O")
             _close(lse.reshape(B, Hq, Lq), l_ref, 1e-12, "combine LSE")
 
@@ -303,14 +312,18 @@ def pin_varlen_equals_per_sequence(mutant=0):
     k = r.standard_normal((cu_k[-1], Hkv, d))
     v = r.standard_normal((cu_k[-1], Hkv, d))
     sink = r.standard_normal(Hq)
-    o, lse = oracle.attn_varlen(q, k, v, cu_q, cu_k, 0.5, True, 0.7, sink, mutant=mutant)
-    for b in range(3):
-        qs = q[cu_q[b]:cu_q[b + 1]].transpose(1, 0, 2)[None]
-        ks = k[cu_k[b]:cu_k[b + 1]].transpose(1, 0, 2)[None]
-        vs = v[cu_k[b]:cu_k[b + 1]].transpose(1, 0, 2)[None]
-        od, ld = oracle.attn_dense(qs, ks, vs, 0.5, True, 0.7, sink, mutant=mutant)
-        _close(o[cu_q[b]:cu_q[b + 1]].transpose(1, 0, 2), od[0], 0.0, "varlen O")
-        _close(lse[:, cu_q[b]:cu_q[b + 1]], ld[0], 0.0, "varlen LSE")
+    slopes = np.abs(r.standard_normal((3, Hq)))
+    for tl, al in ((False, None), (True, slopes), (False, slopes)):
+        o, lse = oracle.attn_varlen(q, k, v, cu_q, cu_k, 0.5, True, 0.7, sink, mutant=mutant,
+                                    top_left=tl, alibi=al)
+        for b in range(3):
+            qs = q[cu_q[b]:cu_q[b + 1]].transpose(1, 0, 2)[None]
+            ks = k[cu_k[b]:cu_k[b + 1]].transpose(1, 0, 2)[None]
+            vs = v[cu_k[b]:cu_k[b + 1]].transpose(1, 0, 2)[None]
+            od, ld = oracle.attn_dense(qs, ks, vs, 0.5, True, 0.7, sink, mutant=mutant,
+                                       top_left=tl, alibi=None if al is None else al[b:b + 1])
+            _close(o[cu_q[b]:cu_q[b + 1]].transpose(1, 0, 2), od[0], 0.0, "varlen O")
+            _close(lse[:, cu_q[b]:cu_q[b + 1]], ld[0], 0.0, "varlen LSE")
 
 
 def pin_window(mutant=0):
@@ -346,10 +359,75 @@ def pin_window(mutant=0):
     _close(l3, 0.5 * np.einsum("bhid,bhid->bhi", q, k[:, :, 3:10]), 1e-14, "width-one LSE")
 
 
+def pin_bias_alibi_top_left(mutant=0):
+    """Additive bias, ALiBi and the top-left mask alignment (Composable Kernel
+    FMHA forward: bias kargs, ALiBi slope per (batch, head) aligned like the
+    mask, MASK_FROM_TOP_LEFT): brute force agrees; a per-row constant bias only
+    shifts the LSE; a bias of -inf above the diagonal is the causal mask; ALiBi
+    equals the explicit bias -slope*|diag - j| built here; a two-key closed form
+    fixes the ALiBi sign; top-left equals bottom-right when Lq = Lk and keeps
+    only key 0 for row 0 under causal."""
+    r = _rng(21)
+    for (Lq, Lk, causal, win, tl) in ((5, 7, True, (-1, -1), False), (7, 5, True, (-1, -1), True),
+                                      (6, 6, False, (2, 1), True), (4, 9, False, (-1, -1), False)):
+        q = r.standard_normal((2, 2, Lq, 4))
+        k = r.standard_normal((2, 1, Lk, 4))
+        v = r.standard_normal((2, 1, Lk, 4))
+        al = np.abs(r.standard_normal((2, 2))) * 0.3
+        bias = r.standard_normal((2, 2, Lq, Lk))
+        o, lse = oracle.attn_dense(q, k, v, 0.5, causal, mutant=mutant, window=win, top_left=tl,
+                                   alibi=al, bias=bias)
+        bo, bl = _brute.dense(q.tolist(), k.tolist(), v.tolist(), 0.5, causal, window=win,
+                              top_left=tl, alibi=al.tolist(), bias=bias.tolist())
+        _close(o, np.array(bo), 1e-12, f"bias/alibi brute O {Lq, Lk, causal, win, tl}")
+        _close(lse, np.array(bl), 1e-12, f"bias/alibi brute LSE {Lq, Lk, causal, win, tl}")
+    q = r.standard_normal((1, 2, 6, 4))
+    k = r.standard_normal((1, 2, 8, 4))
+    v = r.standard_normal((1, 2, 8, 4))
+    o0, l0 = oracle.attn_dense(q, k, v, 0.5, mutant=mutant)
+    c = r.standard_normal((1, 2, 6, 1))
+    o1, l1 = oracle.attn_dense(q, k, v, 0.5, mutant=mutant, bias=np.broadcast_to(c, (1, 2, 6, 8)))
+    _close(o1, o0, 1e-13, "row-constant bias leaves O")
+    _close(l1, l0 + c[..., 0], 1e-13, "row-constant bias shifts LSE")
+    i = np.arange(6)[:, None]
+    j = np.arange(8)[None, :]
+    diag = i + (8 - 6)
+    neg = np.where(j > diag, -np.inf, 0.0)
+    oc, lc = oracle.attn_dense(q, k, v, 0.5, causal=True, mutant=mutant)
+    o2, l2 = oracle.attn_dense(q, k, v, 0.5, mutant=mutant, bias=neg)
+    _close(o2, oc, 1e-13, "-inf bias above the diagonal is causal")
+    _close(l2, lc, 1e-13, "-inf bias above the diagonal is causal, LSE")
+    slopes = np.array([[0.25, 0.7]])
+    explicit = -slopes[0][None, :, None, None] * np.abs(diag - j)[None, None]
+    o3, l3 = oracle.attn_dense(q, k, v, 0.5, mutant=mutant, alibi=slopes)
+    o4, l4 = oracle.attn_dense(q, k, v, 0.5, mutant=mutant, bias=explicit)
+    _close(o3, o4, 1e-13, "ALiBi equals its explicit bias")
+    _close(l3, l4, 1e-13, "ALiBi equals its explicit bias, LSE")
+    o5, _ = oracle.attn_dense(q, k, v, 0.5, mutant=mutant, alibi=np.zeros((1, 2)))
+    _close(o5, o0, 0.0, "zero slope is no ALiBi")
+    # Two identical keys, one query on the diagonal of key 1 (bottom-right):
+    # weights e^{-m} (key 0, distance 1) and 1 (key 1).
+    m = 0.9
+    kk = np.ones((1, 1, 2, 4))
+    vv = np.array([[[[1.0, 0, 0, 0], [0, 1.0, 0, 0]]]])
+    qq = np.ones((1, 1, 1, 4))
+    o6, l6 = oracle.attn_dense(qq, kk, vv, 0.5, mutant=mutant, alibi=np.array([[m]]))
+    w0 = math.exp(-m) / (math.exp(-m) + 1.0)
+    _close(o6[0, 0, 0], [w0, 1.0 - w0, 0, 0], 1e-14, "ALiBi two-key closed form")
+    _close(l6[0, 0, 0], 2.0 + math.log(math.exp(-m) + 1.0), 1e-14, "ALiBi two-key LSE")
+    ob, lb = oracle.attn_dense(q[:, :, :6], k[:, :, :6], v[:, :, :6], 0.5, causal=True,
+                               mutant=mutant)
+    ot, lt = oracle.attn_dense(q[:, :, :6], k[:, :, :6], v[:, :, :6], 0.5, causal=True,
+                               mutant=mutant, top_left=True)
+    _close(ot, ob, 0.0, "top-left equals bottom-right when Lq = Lk")
+    o7, _ = oracle.attn_dense(q, k, v, 0.5, causal=True, mutant=mutant, top_left=True)
+    _close(o7[:, :, 0], v[:, :, 0], 1e-14, "top-left causal row 0 is V[0]")
+
+
 PINS = [pin_golden, pin_rows_sum_to_one, pin_identical_keys, pin_one_hot, pin_lse_fsum,
         pin_causal_row0, pin_empty_rows, pin_brute_force, pin_softcap_limits, pin_sink_limits,
         pin_gqa_equals_repeated_mha, pin_paged_equals_contiguous, pin_splits_combine_to_unsplit,
-        pin_varlen_equals_per_sequence, pin_window]
+        pin_varlen_equals_per_sequence, pin_window, pin_bias_alibi_top_left]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
