@@ -57,7 +57,7 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _opts(scale, causal, softcap, sink, window=None):
+def _opts(scale, causal, softcap, sink, window=None, top_left=False, alibi=None, bias=None):
     o = _lib.attn_opts()
     o.scale = float(scale) if scale is not None else 0.0
     o.causal = 1 if causal else 0
@@ -66,7 +66,33 @@ def _opts(scale, causal, softcap, sink, window=None):
     if window is not None:
         o.use_window = 1
         o.window_left, o.window_right = int(window[0]), int(window[1])
+    o.top_left = 1 if top_left else 0
+    if alibi is not None:
+        o.alibi_slopes = alibi.data_ptr()
+        o.alibi_stride = 0 if alibi.dim() == 1 else int(alibi.stride(0))
+    if bias is not None:
+        o.bias = bias.data_ptr()
+        o.bias_strides = _lib.attn_strides(*_bias_strides(bias))
     return o
+
+
+def _check_alibi(alibi, B, Hq, device):
+    """ALiBi slopes: fp32 [Hq] (shared by every batch) or [B, Hq] (row-contiguous)."""
+    if alibi is None:
+        return None
+    if alibi.dtype != torch.float32 or alibi.device != device or alibi.stride(-1) != 1 or \
+            alibi.shape[-1] != Hq or alibi.dim() not in (1, 2) or \
+            (alibi.dim() == 2 and alibi.shape[0] != B):
+        raise ValueError("alibi_slopes must be fp32 [Hq] or [B, Hq] on the same device")
+    return alibi
+
+
+def _bias_strides(bias):
+    """(batch, head, row) element strides of a bias viewed as [B, Hq, Lq, Lk]
+    (size-1 broadcast dimensions get stride 0)."""
+    if bias.dim() != 4 or bias.stride(3) != 1:
+        raise ValueError("bias must be 4-D [B|1, Hq|1, Lq, Lk] with a unit key stride")
+    return tuple(0 if bias.shape[i] == 1 else bias.stride(i) for i in range(3))
 
 
 def _strides_bhld(t):
@@ -92,10 +118,12 @@ def _check_sink(sink, Hq, device):
 
 
 def attn_fwd(q, k, v, o=None, lse=True, causal=False, scale=None, softcap=0.0, sink=None,
-             stream=None, window=None):
+             stream=None, window=None, top_left=False, alibi_slopes=None, bias=None):
     """Dense attention.  q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] (any strides with d-stride 1).
     ``window`` = (left, right) keeps keys i+Lk-Lq-left <= j <= i+Lk-Lq+right (a
-    negative side is unbounded).  Returns (o [B,Hq,Lq,d], lse fp32 [B,Hq,Lq] or None)."""
+    negative side is unbounded); ``top_left`` drops the Lk-Lq shift.
+    ``alibi_slopes``: fp32 [Hq] or [B,Hq]; ``bias``: [B|1,Hq|1,Lq,Lk] in the input
+    dtype, added to the scaled score.  Returns (o [B,Hq,Lq,d], lse fp32 [B,Hq,Lq] or None)."""
     B, Hq, Lq, d = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     if o is None:
@@ -106,7 +134,10 @@ def attn_fwd(q, k, v, o=None, lse=True, causal=False, scale=None, softcap=0.0, s
     elif isinstance(lse, torch.Tensor):
         lse_t = lse
     sink = _check_sink(sink, Hq, q.device)
-    opts = _opts(scale, causal, softcap, sink, window)
+    alibi_slopes = _check_alibi(alibi_slopes, B, Hq, q.device)
+    if bias is not None and (bias.dtype != q.dtype or bias.device != q.device):
+        raise ValueError("bias must have the input dtype and device")
+    opts = _opts(scale, causal, softcap, sink, window, top_left, alibi_slopes, bias)
     st = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, Hq, Hkv, Lq, Lk,
                             d, _dtype_code(q), _strides_bhld(q), _strides_bhld(k),
                             _strides_bhld(v), _strides_bhld(o), ctypes.byref(opts),
@@ -116,7 +147,8 @@ def attn_fwd(q, k, v, o=None, lse=True, causal=False, scale=None, softcap=0.0, s
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, o=None, lse=True,
-                    causal=False, scale=None, softcap=0.0, sink=None, stream=None, window=None):
+                    causal=False, scale=None, softcap=0.0, sink=None, stream=None, window=None,
+                    top_left=False, alibi_slopes=None):
     """Group mode.  q [total_q,Hq,d], k/v [total_k,Hkv,d], cu_seqlens int32 [B+1] on the
     device.  Returns (o [total_q,Hq,d], lse fp32 [Hq,total_q] or None)."""
     total_q, Hq, d = q.shape
@@ -133,7 +165,8 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, o=None, l
     elif isinstance(lse, torch.Tensor):
         lse_t = lse
     sink = _check_sink(sink, Hq, q.device)
-    opts = _opts(scale, causal, softcap, sink, window)
+    alibi_slopes = _check_alibi(alibi_slopes, B, Hq, q.device)
+    opts = _opts(scale, causal, softcap, sink, window, top_left, alibi_slopes)
     st = library().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t),
                                    _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, total_q, total_k,
                                    int(max_seqlen_q), Hq, Hkv, d, _dtype_code(q),
@@ -151,16 +184,17 @@ def attn_paged_auto_splits(B, Hkv, max_pages_per_seq) -> int:
     return int(library().attn_paged_auto_splits(B, Hkv, max_pages_per_seq))
 
 
-def attn_paged_window_pages(Lq, page_size, max_pages_per_seq, window=None, causal=False) -> int:
+def attn_paged_window_pages(Lq, page_size, max_pages_per_seq, window=None, causal=False,
+                            top_left=False) -> int:
     """Pages of one sequence the paged split layout tiles (W of attn_fwd_paged)."""
-    opts = _opts(None, causal, 0.0, None, window)
+    opts = _opts(None, causal, 0.0, None, window, top_left)
     return int(library().attn_paged_window_pages(Lq, page_size, max_pages_per_seq,
                                                  ctypes.byref(opts)))
 
 
 def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=None, lse=True,
                    causal=False, scale=None, softcap=0.0, sink=None, workspace=None,
-                   stream=None, window=None):
+                   stream=None, window=None, top_left=False, alibi_slopes=None):
     """Paged KV.  q [B,Lq,Hq,d], pools [num_pages,page,Hkv,d], block_table int32
     [B,max_pages], seqlens_k int32 [B] (all on the device, contiguous).
     Returns (o [B,Lq,Hq,d], lse fp32 [B,Hq,Lq] or None)."""
@@ -172,7 +206,7 @@ def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=No
             raise ValueError("paged inputs must be contiguous")
     if num_splits == 0:
         num_splits = attn_paged_auto_splits(
-            B, Hkv, attn_paged_window_pages(Lq, page, max_pages, window, causal))
+            B, Hkv, attn_paged_window_pages(Lq, page, max_pages, window, causal, top_left))
     if o is None:
         o = torch.empty((B, Lq, Hq, d), dtype=q.dtype, device=q.device)
     lse_t = None
@@ -189,7 +223,8 @@ def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=No
         o_part = workspace[: num_splits * rows * d]
         lse_part = workspace[num_splits * rows * d: need]
     sink = _check_sink(sink, Hq, q.device)
-    opts = _opts(scale, causal, softcap, sink, window)
+    alibi_slopes = _check_alibi(alibi_slopes, B, Hq, q.device)
+    opts = _opts(scale, causal, softcap, sink, window, top_left, alibi_slopes)
     st = library().attn_fwd_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
                                   _ptr(seqlens_k), _ptr(o), _ptr(lse_t), B, Lq, Hq, Hkv, d,
                                   _dtype_code(q), page, num_pages, max_pages, num_splits,
@@ -201,7 +236,7 @@ def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=No
 
 def attn_fwd_paged_noalloc(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=None,
                            lse=True, causal=False, scale=None, softcap=0.0, sink=None,
-                           stream=None, window=None):
+                           stream=None, window=None, top_left=False, alibi_slopes=None):
     """attn_fwd_paged for callers that cannot allocate device scratch: the split
     partials live in a fixed 16 MiB array inside the library (shared by all
     calls on a GPU; calls overlapping on the GPU race).  Outputs are allocated
@@ -216,7 +251,8 @@ def attn_fwd_paged_noalloc(q, k_pool, v_pool, block_table, seqlens_k, num_splits
     elif isinstance(lse, torch.Tensor):
         lse_t = lse
     sink = _check_sink(sink, Hq, q.device)
-    opts = _opts(scale, causal, softcap, sink, window)
+    alibi_slopes = _check_alibi(alibi_slopes, B, Hq, q.device)
+    opts = _opts(scale, causal, softcap, sink, window, top_left, alibi_slopes)
     st = library().attn_fwd_paged_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
                                           _ptr(seqlens_k), _ptr(o), _ptr(lse_t), B, Lq, Hq, Hkv,
                                           d, _dtype_code(q), page, num_pages,

@@ -19,7 +19,10 @@ class attn_strides(ctypes.Structure):
 class attn_opts(ctypes.Structure):
     _fields_ = [("scale", ctypes.c_float), ("causal", ctypes.c_int), ("softcap", ctypes.c_float),
                 ("sink", ctypes.c_void_p), ("use_window", ctypes.c_int),
-                ("window_left", ctypes.c_int), ("window_right", ctypes.c_int)]
+                ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("top_left", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
+                ("alibi_stride", ctypes.c_int), ("bias", ctypes.c_void_p),
+                ("bias_strides", attn_strides)]
 
 
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",

@@ -129,8 +129,63 @@ void fill_common(PrefillParams& p, const attn_opts* opts, int d) {
   p.softcap_inv = cap > 0.0f ? 1.0f / cap : 0.0f;
   p.sink = opts != nullptr ? opts->sink : nullptr;
   resolve_window(opts, &p.win_left, &p.win_right);
+  p.top_left = (opts != nullptr && opts->top_left) ? 1 : 0;
+  p.inv_scale = 1.0f / scale;
+  p.alibi = opts != nullptr ? opts->alibi_slopes : nullptr;
+  p.alibi_stride = opts != nullptr ? opts->alibi_stride : 0;
   p.timeout_ns = kTimeoutNs;
 }
+
+// Options every entry point checks: pointer alignment of the per-head
+// vectors, and the combinations the pages leave undefined or that are not
+// built (soft-cap with ALiBi or bias: the order is not on the pages; ALiBi
+// with a bias: the Composable Kernel bias kind is one or the other).
+attn_status check_opts(const attn_opts* opts, int Hq, bool allow_bias) {
+  if (opts == nullptr) return ATTN_OK;
+  if (opts->sink != nullptr && (reinterpret_cast<uintptr_t>(opts->sink) & 3u))
+    return ATTN_ERR_INVALID;
+  const bool alibi = opts->alibi_slopes != nullptr, bias = opts->bias != nullptr;
+  if (alibi && ((reinterpret_cast<uintptr_t>(opts->alibi_slopes) & 3u) ||
+                (opts->alibi_stride != 0 && opts->alibi_stride < Hq)))
+    return ATTN_ERR_INVALID;
+  if (bias && !allow_bias) return ATTN_ERR_UNSUPPORTED;
+  if ((alibi || bias) && opts->softcap > 0.0f) return ATTN_ERR_UNSUPPORTED;
+  if (alibi && bias) return ATTN_ERR_UNSUPPORTED;
+  if (bias) {
+    const attn_strides& b = opts->bias_strides;
+    if (!aligned16(opts->bias) || b.row < 0 || b.head < 0 || b.batch < 0 || (b.row % 8) ||
+        (b.head % 8) || (b.batch % 8))
+      return ATTN_ERR_INVALID;
+  }
+  return ATTN_OK;
+}
+
+int score_xf(const PrefillParams& p) {
+  if (p.softcap > 0.0f) return kXfSoftcap;
+  if (p.alibi != nullptr) return kXfAlibi;
+  if (p.bias != nullptr) return kXfBias;
+  return kXfNone;
+}
+
+}  // namespace
+
+namespace attn {
+cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool masked,
+                           int xf, cudaStream_t stream, char* name, size_t name_len) {
+  const char* mask = !masked ? "nomask"
+                     : (p.win_left < 0 && p.win_right == 0) ? "causal"
+                                                            : "window";
+  static const char* const kXfName[4] = {"plain", "softcap", "alibi", "bias"};
+  snprintf(name, name_len, "attn_prefill_tcgen05_d%d_%s_%s%s_%s_m256n128_persistent", d,
+           bf16 ? "bf16" : "f16", mask, p.top_left ? "_topleft" : "",
+           kXfName[(xf >= 0 && xf < 4) ? xf : 0]);
+  if (d == 64) return launch_prefill_d<64>(p, grid, bf16, masked, xf, stream);
+  if (d == 128) return launch_prefill_d<128>(p, grid, bf16, masked, xf, stream);
+  return cudaErrorInvalidValue;
+}
+}  // namespace attn
+
+namespace {
 
 attn_status finish_launch(cudaError_t e) {
   if (e != cudaSuccess) {
@@ -223,8 +278,10 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     return ATTN_ERR_INVALID;
   for (const attn_strides* s : {&sq, &sk, &sv, &so})
     if (!stride_ok(s->row) || !stride_ok(s->head) || !stride_ok(s->batch)) return ATTN_ERR_INVALID;
-  if (opts != nullptr && opts->sink != nullptr && (reinterpret_cast<uintptr_t>(opts->sink) & 3u))
-    return ATTN_ERR_INVALID;
+  {
+    const attn_status so_ = check_opts(opts, Hq, true);
+    if (so_ != ATTN_OK) return so_;
+  }
   if (static_cast<int64_t>(B) * Hq * ((Lq + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
 
   PrefillParams p;
@@ -269,10 +326,16 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.num_m_blocks = (Lq + 255) / 256;
   p.err = err;
   fill_common(p, opts, d);
+  if (opts != nullptr && opts->bias != nullptr) {
+    p.bias = opts->bias;
+    p.bias_row = opts->bias_strides.row;
+    p.bias_head = opts->bias_strides.head;
+    p.bias_batch = opts->bias_strides.batch;
+  }
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
   p.num_items = p.num_m_blocks * B * Hq;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
-  return finish_launch(launch_prefill(p, grid, d, bf16, masked, p.softcap > 0.0f,
+  return finish_launch(launch_prefill(p, grid, d, bf16, masked, score_xf(p),
                                       static_cast<cudaStream_t>(stream), g_last_name,
                                       sizeof(g_last_name)));
 }
@@ -298,6 +361,10 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
     if (!stride_ok(s->row) || !stride_ok(s->head)) return ATTN_ERR_INVALID;
   if (static_cast<int64_t>(B) * Hq * ((max_seqlen_q + 255) / 256) > 0x7fffffffLL)
     return ATTN_ERR_UNSUPPORTED;
+  {
+    const attn_status so_ = check_opts(opts, Hq, false);
+    if (so_ != ATTN_OK) return so_;
+  }
 
   PrefillParams p;
   memset(&p, 0, sizeof(p));
@@ -349,7 +416,7 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
   p.num_items = p.num_m_blocks * B * Hq;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
-  return finish_launch(launch_prefill(p, grid, d, bf16, masked, p.softcap > 0.0f,
+  return finish_launch(launch_prefill(p, grid, d, bf16, masked, score_xf(p),
                                       static_cast<cudaStream_t>(stream), g_last_name,
                                       sizeof(g_last_name)));
 }
@@ -363,7 +430,10 @@ size_t attn_paged_workspace_bytes(int B, int Lq, int Hq, int d, int num_splits) 
 int attn_paged_window_pages(int Lq, int page_size, int max_pages_per_seq, const attn_opts* opts) {
   int wl = -1, wr = -1;
   resolve_window(opts, &wl, &wr);
-  if (wl < 0 || Lq < 0 || page_size <= 0 || max_pages_per_seq <= 0) return max_pages_per_seq;
+  // Top-left bands start at key 0: no saving is claimed for them.
+  if (wl < 0 || Lq < 0 || page_size <= 0 || max_pages_per_seq <= 0 ||
+      (opts != nullptr && opts->top_left))
+    return max_pages_per_seq;
   const int64_t w = (static_cast<int64_t>(Lq) + wl + page_size - 1) / page_size + 1;
   return w < max_pages_per_seq ? static_cast<int>(w) : max_pages_per_seq;
 }
@@ -440,6 +510,10 @@ attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool
       (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return ATTN_ERR_INVALID;
   if (B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  {
+    const attn_status so_ = check_opts(opts, Hq, false);
+    if (so_ != ATTN_OK) return so_;
+  }
   const int win_pages = attn_paged_window_pages(Lq, page_size, max_pages_per_seq, opts);
   if (num_splits == 0) num_splits = attn_paged_auto_splits(B, Hkv, win_pages);
   if (num_splits > 1 && (o_partial == nullptr || lse_partial == nullptr ||
@@ -481,6 +555,9 @@ attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool
   p.softcap = (opts != nullptr && opts->softcap > 0.0f) ? opts->softcap : 0.0f;
   p.softcap_inv = p.softcap > 0.0f ? 1.0f / p.softcap : 0.0f;
   resolve_window(opts, &p.win_left, &p.win_right);
+  p.top_left = (opts != nullptr && opts->top_left) ? 1 : 0;
+  p.alibi = opts != nullptr ? opts->alibi_slopes : nullptr;
+  p.alibi_stride = opts != nullptr ? opts->alibi_stride : 0;
   p.err = err;
   p.timeout_ns = kTimeoutNs;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);

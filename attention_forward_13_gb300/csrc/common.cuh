@@ -30,6 +30,10 @@ enum ErrBits : uint32_t {
   kErrSelftest = 20,
 };
 
+// Score transform of a prefill instantiation (applied to the raw score
+// before masking).
+enum ScoreXf : int { kXfNone = 0, kXfSoftcap = 1, kXfAlibi = 2, kXfBias = 3 };
+
 // Prefill (dense / varlen) launch parameters.  Tensor maps are 4-D
 // (d, rows, heads, batch); varlen problems use one batch slot and a row base.
 struct PrefillParams {
@@ -55,6 +59,12 @@ struct PrefillParams {
   // <= j <= i + Lk - Lq + win_right; a negative bound is unbounded.  Causal
   // masking is win_right = 0.  Only read by the masked instantiations.
   int win_left, win_right;
+  int top_left;                    // masks and ALiBi aligned top-left (row i on key i)
+  float inv_scale;                 // 1 / scale (bias and ALiBi go to raw-score units)
+  const float* alibi;              // ALiBi slopes, (b, h) at b * alibi_stride + h
+  int alibi_stride;
+  const void* bias;                // elementwise bias (input dtype), batch mode only
+  int64_t bias_row, bias_head, bias_batch;  // its element strides (key stride 1)
   unsigned int* err;
   uint64_t timeout_ns;
 };
@@ -74,6 +84,9 @@ struct DecodeParams {
   int B, Lq, Hq, Hkv, page_size, num_pages, max_pages, num_splits, chunk_pages;
   float scale_log2, scale, softcap, softcap_inv;
   int win_left, win_right;  // as in PrefillParams (causal is win_right = 0)
+  int top_left;
+  const float* alibi;       // ALiBi slopes as in PrefillParams, or nullptr
+  int alibi_stride;
   unsigned int* err;
   uint64_t timeout_ns;
 };

@@ -138,7 +138,8 @@ __global__ void __launch_bounds__(192, 2)
   // With a left window the splits tile only the pages holding kept keys:
   // every row's right bound reaches the last key, the first row's left bound
   // is the lowest.
-  const int k_lo = p.win_left >= 0 ? max(0, L - p.Lq - p.win_left) : 0;
+  const int diag0 = p.top_left ? 0 : L - p.Lq;  // key on query row 0's diagonal
+  const int k_lo = p.win_left >= 0 ? max(0, diag0 - p.win_left) : 0;
   const int pg0 = k_lo / P + split * p.chunk_pages;
   const int pg1 = min(pg0 + p.chunk_pages, pages_b);
   const int k0 = pg0 * P;
@@ -360,7 +361,15 @@ __global__ void __launch_bounds__(192, 2)
       m_use[r] = -INFINITY;
       lpart[r] = 0.0f;
     }
-    const int diag = L - p.Lq;  // bottom-right mask offset within the sequence
+    const int diag = diag0;  // key on query row 0's diagonal (bottom-right unless top-left)
+    // ALiBi slope of each row's query head, in log2 units (CK position
+    // encoding: -slope * |diag(i) - j| on the natural-log score).
+    float al[C::NR];
+#pragma unroll
+    for (int r = 0; r < C::NR; ++r) {
+      const int h = hk * g + (r % g);
+      al[r] = (p.alibi != nullptr && r < R) ? p.alibi[b * p.alibi_stride + h] * kLog2e : 0.0f;
+    }
     // Every thread runs every iteration and every named barrier even after a
     // timeout (waits then return at once), so the four warps never part ways
     // at a barrier.
@@ -388,6 +397,7 @@ __global__ void __launch_bounds__(192, 2)
         } else {
           s *= p.scale_log2;
         }
+        if (p.alibi != nullptr) s = fmaf(-al[r], fabsf(static_cast<float>((r / g) + diag - key)), s);
         bool valid = (key < k1) && (r < R);
         if (p.win_right >= 0) valid = valid && (key <= (r / g) + diag + p.win_right);
         if (p.win_left >= 0) valid = valid && (key >= (r / g) + diag - p.win_left);

@@ -7,9 +7,15 @@
 
 namespace attn {
 
-// grid = number of CTAs; name receives the kernel's trait string.
+// grid = number of CTAs; name receives the kernel's trait string.  xf is a
+// ScoreXf value.  Dispatches to launch_prefill_d<64 / 128>.
 cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool masked,
-                           bool softcap, cudaStream_t stream, char* name, size_t name_len);
+                           int xf, cudaStream_t stream, char* name, size_t name_len);
+// One per head dimension, each in its own translation unit (prefill_d64.cu,
+// prefill_d128.cu) so the two compile in parallel.
+template <int D>
+cudaError_t launch_prefill_d(const PrefillParams& p, int grid, bool bf16, bool masked, int xf,
+                             cudaStream_t stream);
 
 cudaError_t launch_decode(const DecodeParams& p, int d, bool bf16, bool softcap, int rows,
                           cudaStream_t stream, char* name, size_t name_len);

@@ -1,5 +1,6 @@
-// prefill.cu -- fused attention forward for dense and varlen (group-mode)
-// problems on sm_103a: TMA loads into 128B-swizzled shared memory behind
+// prefill_kernel.cuh -- fused attention forward for dense and varlen
+// (group-mode) problems on sm_103a, compiled once per head dimension
+// (prefill_d64.cu, prefill_d128.cu define ATTN_PREFILL_D and include this): TMA loads into 128B-swizzled shared memory behind
 // mbarrier rings, S = Q K^T and O += P V on the 5th-generation tensor cores
 // (tcgen05.mma, accumulators in tensor memory), online softmax in registers.
 //
@@ -30,6 +31,7 @@
 //  * every mbarrier wait is bounded (Waiter): a CTA that gives up records a
 //    bit in the device error word, drains its own copies and MMAs, frees its
 //    tensor memory and returns.
+#pragma once
 #include "ptx.cuh"
 #include "common.cuh"
 #include "launch.h"
@@ -128,6 +130,41 @@ __device__ __forceinline__ void tanh128(float* s, float in_scale) {
   }
 }
 
+// Adds inv_scale * bias[c] to the raw scores s[c], c < min(128, nvalid)
+// (columns past the key end are masked afterwards).  Whole 16-byte loads
+// where the 8 keys exist, element loads at the ragged end.
+template <bool BF16>
+__device__ __forceinline__ void add_bias_row(float* s, const void* src, int nvalid,
+                                             float inv_scale) {
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  const T* b = reinterpret_cast<const T*>(src);
+#pragma unroll
+  for (int c8 = 0; c8 < 16; ++c8) {
+    if (8 * c8 + 8 <= nvalid) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(b + 8 * c8));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float lo, hi;
+        if constexpr (BF16) {
+          lo = __uint_as_float(w[i] << 16);
+          hi = __uint_as_float(w[i] & 0xffff0000u);
+        } else {
+          const __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
+          lo = __low2float(h2);
+          hi = __high2float(h2);
+        }
+        s[8 * c8 + 2 * i] = fmaf(lo, inv_scale, s[8 * c8 + 2 * i]);
+        s[8 * c8 + 2 * i + 1] = fmaf(hi, inv_scale, s[8 * c8 + 2 * i + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (8 * c8 + i < nvalid) s[8 * c8 + i] = fmaf(static_cast<float>(b[8 * c8 + i]), inv_scale, s[8 * c8 + i]);
+    }
+  }
+}
+
 // Wait for a barrier phase ignoring the abort flag (teardown only).
 __device__ __forceinline__ bool wait_raw(uint64_t* bar, uint32_t parity, uint64_t deadline) {
   while (!mbar_try_wait(bar, parity)) {
@@ -180,7 +217,7 @@ __device__ __forceinline__ bool decode_item(const PrefillParams& p, int item, Pr
   }
   it.m0 = mb * 2 * BM;
   if (it.m0 >= it.Lq) return false;
-  const int diag = it.Lk - it.Lq;
+  const int diag = p.top_left ? 0 : it.Lk - it.Lq;  // key on row 0's diagonal
   int tb[2], te[2];  // K/V tile range [tb, te) of each query tile
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
@@ -217,7 +254,9 @@ __device__ __forceinline__ int item_of_round(int r) {
   return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-template <int D, bool BF16, bool MASK, bool SOFTCAP>
+// XF: score transform before masking (ScoreXf): none, soft-cap, ALiBi or an
+// elementwise bias (the last two are mutually exclusive with the soft-cap).
+template <int D, bool BF16, bool MASK, int XF>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = PrefillCfg<D>;
@@ -416,8 +455,14 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       if (mt >= it.Lq) continue;  // this tile has no row
       const int qi = mt + r;      // query index within the sequence
       const int nt = it.ue[t] - it.ub[t];  // K/V steps of this tile
-      const int diag = it.Lk - it.Lq;      // bottom-right alignment offset
+      const int diag = p.top_left ? 0 : it.Lk - it.Lq;  // key on row 0's diagonal
       const int last = min(mt + C::BM - 1, it.Lq - 1);
+      float alibi_raw = 0.0f;      // ALiBi slope / scale (raw-score units)
+      const T* bias_row = nullptr;  // this row's bias, key 0
+      if constexpr (XF == kXfAlibi) alibi_raw = p.alibi[it.b * p.alibi_stride + it.h] * p.inv_scale;
+      if constexpr (XF == kXfBias)
+        bias_row = reinterpret_cast<const T*>(p.bias) + it.b * p.bias_batch + it.h * p.bias_head +
+                   static_cast<int64_t>(qi) * p.bias_row;
 
       float m_use = -INFINITY;  // exp2 subtrahend currently in use (log2 units)
       float l = 0.0f;           // running denominator w.r.t. m_use
@@ -444,11 +489,21 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         // is folded into the exponent's FMA (CK MakeKargs FAST_EXP2 fold).
         float* s = reinterpret_cast<float*>(sr);
         float a_coef = p.scale_log2;
-        if constexpr (SOFTCAP) {
+        const int j0 = (it.jb + it.ub[t] + j) * C::BN;  // first key of this K/V tile
+        if constexpr (XF == kXfSoftcap) {
           tanh128(s, p.scale * p.softcap_inv);
           a_coef = p.softcap * kLog2e;
+        } else if constexpr (XF == kXfAlibi) {
+          // CK ALiBi position encoding (slope per (batch, head), aligned like
+          // the mask): natural-log score - slope*|diag - j|, in raw-score
+          // units (divided by the scale folded in later).
+          const int dq = qi + diag - j0;  // this row's diagonal, as a column
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = fmaf(-alibi_raw, fabsf(static_cast<float>(dq - c)), s[c]);
+        } else if constexpr (XF == kXfBias) {
+          // CK elementwise bias (natural-log units, added to the scaled score).
+          if (qi < it.Lq) add_bias_row<BF16>(s, bias_row + j0, it.Lk - j0, p.inv_scale);
         }
-        const int j0 = (it.jb + it.ub[t] + j) * C::BN;  // first key of this K/V tile
         if ((j0 + C::BN > it.Lk) ||
             (MASK && p.win_right >= 0 && j0 + C::BN - 1 > mt + diag + p.win_right) ||
             (MASK && p.win_left >= 0 && j0 < last + diag - p.win_left)) {
@@ -590,10 +645,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool BF16, bool MASK, bool SOFTCAP>
+template <int D, bool BF16, bool MASK, int XF>
 static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream_t stream) {
   using C = PrefillCfg<D>;
-  auto kern = attn_prefill_kernel<D, BF16, MASK, SOFTCAP>;
+  auto kern = attn_prefill_kernel<D, BF16, MASK, XF>;
   const int smem = static_cast<int>(sizeof(PrefillSmem<C>)) + 1024;
   static bool configured = false;  // per instantiation; attribute set is idempotent
   if (!configured) {
@@ -605,34 +660,25 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool masked,
-                           bool softcap, cudaStream_t stream, char* name, size_t name_len) {
-  const char* mask = !masked ? "nomask"
-                     : (p.win_left < 0 && p.win_right == 0) ? "causal"
-                                                            : "window";
-  snprintf(name, name_len, "attn_prefill_tcgen05_d%d_%s_%s_%s_m256n128_persistent", d,
-           bf16 ? "bf16" : "f16", mask, softcap ? "softcap" : "nocap");
-#define ATTN_PREFILL_CASE(D_, B_, C_, S_)                                        \
-  if (d == D_ && bf16 == B_ && masked == C_ && softcap == S_)                    \
-    return launch_prefill_t<D_, B_, C_, S_>(p, grid, stream);
-  ATTN_PREFILL_CASE(64, true, false, false)
-  ATTN_PREFILL_CASE(64, true, false, true)
-  ATTN_PREFILL_CASE(64, true, true, false)
-  ATTN_PREFILL_CASE(64, true, true, true)
-  ATTN_PREFILL_CASE(64, false, false, false)
-  ATTN_PREFILL_CASE(64, false, false, true)
-  ATTN_PREFILL_CASE(64, false, true, false)
-  ATTN_PREFILL_CASE(64, false, true, true)
-  ATTN_PREFILL_CASE(128, true, false, false)
-  ATTN_PREFILL_CASE(128, true, false, true)
-  ATTN_PREFILL_CASE(128, true, true, false)
-  ATTN_PREFILL_CASE(128, true, true, true)
-  ATTN_PREFILL_CASE(128, false, false, false)
-  ATTN_PREFILL_CASE(128, false, false, true)
-  ATTN_PREFILL_CASE(128, false, true, false)
-  ATTN_PREFILL_CASE(128, false, true, true)
-#undef ATTN_PREFILL_CASE
-  return cudaErrorInvalidValue;
+template <bool BF16, bool MASK>
+static cudaError_t launch_prefill_x(const PrefillParams& p, int grid, int xf,
+                                   cudaStream_t stream) {
+  switch (xf) {
+    case kXfNone: return launch_prefill_t<ATTN_PREFILL_D, BF16, MASK, kXfNone>(p, grid, stream);
+    case kXfSoftcap: return launch_prefill_t<ATTN_PREFILL_D, BF16, MASK, kXfSoftcap>(p, grid, stream);
+    case kXfAlibi: return launch_prefill_t<ATTN_PREFILL_D, BF16, MASK, kXfAlibi>(p, grid, stream);
+    case kXfBias: return launch_prefill_t<ATTN_PREFILL_D, BF16, MASK, kXfBias>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <>
+cudaError_t launch_prefill_d<ATTN_PREFILL_D>(const PrefillParams& p, int grid, bool bf16,
+                                             bool masked, int xf, cudaStream_t stream) {
+  if (bf16) return masked ? launch_prefill_x<true, true>(p, grid, xf, stream)
+                          : launch_prefill_x<true, false>(p, grid, xf, stream);
+  return masked ? launch_prefill_x<false, true>(p, grid, xf, stream)
+                : launch_prefill_x<false, false>(p, grid, xf, stream);
 }
 
 }  // namespace attn

@@ -85,7 +85,23 @@ typedef struct {
   int use_window;    /* nonzero: apply window_left / window_right */
   int window_left;   /* keys kept left of the diagonal (< 0: all) */
   int window_right;  /* keys kept right of the diagonal (< 0: all) */
+  int top_left;      /* nonzero: row i's diagonal is key i (CK MASK_FROM_TOP_LEFT) for the
+                        causal, window and ALiBi terms, instead of key i + Lk - Lq */
+  /* ALiBi (CK position encoding): device fp32 slopes, the slope of (batch b,
+   * query head h) at alibi_slopes[b * alibi_stride + h] (alibi_stride 0: one
+   * [Hq] vector for every batch, else >= Hq).  Adds -slope * |diag(i) - j| to
+   * the scaled score (natural-log units).  NULL: off. */
+  const float* alibi_slopes;
+  int alibi_stride;
+  /* Elementwise bias (CK bias kargs), attn_fwd only: device, the input dtype,
+   * element (b, h, i, j) at bias + b*batch + h*head + i*row + j (strides in
+   * elements, multiples of 8, 0 broadcasts; 16-byte aligned base), added to
+   * the scaled score (natural-log units).  NULL: off. */
+  const void* bias;
+  attn_strides bias_strides;
 } attn_opts;
+/* Combinations not built: soft-cap with ALiBi or bias (the pages do not fix
+ * the order), ALiBi with bias, bias outside attn_fwd: ATTN_ERR_UNSUPPORTED. */
 
 /*
  * attn_fwd -- dense batch mode.

@@ -69,6 +69,36 @@ def test_validation_rejects_before_launch():
     assert _fwd(Lq=0) == 0
 
 
+def test_option_combinations_rejected_before_launch():
+    """Soft-cap with ALiBi or bias, ALiBi with bias, bias outside the dense
+    entry point: ATTN_ERR_UNSUPPORTED; misaligned ALiBi/bias: ATTN_ERR_INVALID."""
+    lib = A.library()
+    p = 1 << 12
+    st = S(1024, 512, 64)
+
+    def dense(**kw):
+        o = _lib.attn_opts()
+        for key, val in kw.items():
+            setattr(o, key, val)
+        return lib.attn_fwd(p, p, p, p, None, 1, 2, 2, 8, 8, 64, 1, st, st, st, st,
+                            ctypes.byref(o), None)
+
+    assert dense(softcap=30.0, alibi_slopes=p) == 2
+    assert dense(softcap=30.0, bias=p, bias_strides=S(0, 0, 8)) == 2
+    assert dense(alibi_slopes=p, bias=p, bias_strides=S(0, 0, 8)) == 2
+    assert dense(alibi_slopes=p + 2) == 1              # misaligned slopes
+    assert dense(alibi_slopes=p, alibi_stride=1) == 1  # stride < Hq
+    assert dense(bias=p + 8, bias_strides=S(0, 0, 8)) == 1  # base not 16-byte aligned
+    assert dense(bias=p, bias_strides=S(0, 0, 12)) == 1     # row stride not a multiple of 8
+    o = _lib.attn_opts()
+    o.bias, o.bias_strides = p, S(0, 0, 8)
+    cu = p
+    assert lib.attn_fwd_varlen(p, p, p, p, None, cu, cu, 1, 8, 8, 8, 2, 2, 64, 1, st, st, st, st,
+                               ctypes.byref(o), None) == 2
+    assert lib.attn_fwd_paged(p, p, p, p, p, p, None, 1, 1, 8, 2, 128, 1, 64, 4, 2, 1, None, None,
+                              ctypes.byref(o), None) == 2
+
+
 def test_paged_validation():
     lib = A.library()
     opts = _lib.attn_opts(0.0, 0, 0.0, None)
