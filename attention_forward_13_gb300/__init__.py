@@ -204,7 +204,9 @@ def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=No
     for t in (q, k_pool, v_pool, block_table, seqlens_k):
         if not t.is_contiguous():
             raise ValueError("paged inputs must be contiguous")
-    if num_splits == 0:
+    if Lq * (Hq // Hkv) > 16:
+        num_splits = 1  # chunked prefill: the prefill kernel, no split-KV scratch
+    elif num_splits == 0:
         num_splits = attn_paged_auto_splits(
             B, Hkv, attn_paged_window_pages(Lq, page, max_pages, window, causal, top_left))
     if o is None:

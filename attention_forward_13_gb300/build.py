@@ -15,9 +15,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libattn_fwd.so")
-SOURCES = ["prefill_d128.cu", "prefill_d64.cu", "decode.cu", "combine.cu", "api.cu",
-           "paged_noalloc.cu"]
-HEADERS = ["ptx.cuh", "common.cuh", "launch.h", "prefill_kernel.cuh"]
+SOURCES = ["prefill_d128.cu", "prefill_d64.cu", "decode_d128.cu", "decode_d64.cu", "combine.cu",
+           "api.cu", "paged_noalloc.cu"]
+HEADERS = ["ptx.cuh", "common.cuh", "launch.h", "prefill_kernel.cuh", "decode_kernel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

@@ -170,6 +170,18 @@ int score_xf(const PrefillParams& p) {
 }  // namespace
 
 namespace attn {
+cudaError_t launch_decode(const DecodeParams& p, int d, bool bf16, bool softcap, int rows,
+                          cudaStream_t stream, char* name, size_t name_len) {
+  const int feat = p.alibi != nullptr ? 2 : (p.win_left >= 0 || p.win_right >= 0) ? 1 : 0;
+  static const char* const kFeat[3] = {"plain", "masked", "alibi"};
+  snprintf(name, name_len, "attn_decode_paged_tcgen05_d%d_%s_%s_%s_rows%d_splits%d", d,
+           bf16 ? "bf16" : "f16", softcap ? "softcap" : "nocap", kFeat[feat], rows,
+           p.num_splits);
+  if (d == 64) return launch_decode_d<64>(p, bf16, softcap, feat, stream);
+  if (d == 128) return launch_decode_d<128>(p, bf16, softcap, feat, stream);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool masked,
                            int xf, cudaStream_t stream, char* name, size_t name_len) {
   const char* mask = !masked ? "nomask"
@@ -421,6 +433,67 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
                                       sizeof(g_last_name)));
 }
 
+}  // extern "C"
+
+namespace {
+// Chunked prefill over a paged KV cache (Lq * g > 16): the prefill kernel with
+// its K/V tiles gathered page by page (Composable Kernel paged-KV kernel,
+// page block navigator with a query tile per CTA).  q/o [B][Lq][Hq][d],
+// lse [B][Hq][Lq]; no split-KV (the query rows give the parallelism).
+attn_status paged_prefill(const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_table, const int32_t* seqlens_k, void* o,
+                          float* lse, int B, int Lq, int Hq, int Hkv, int d, bool bf16,
+                          int page_size, int num_pages, int max_pages, const attn_opts* opts,
+                          cudaStream_t stream) {
+  if (static_cast<int64_t>(B) * Hq * ((Lq + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  unsigned int* err = nullptr;
+  int num_sms = 0;
+  if (device_state(&err, &num_sms) != ATTN_OK) return ATTN_ERR_CUDA;
+  {
+    const uint32_t box[4] = {64, 128, 1, 1};
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lq, (uint64_t)Hq, (uint64_t)B};
+    const uint64_t st[3] = {(uint64_t)Hq * d * 2, (uint64_t)d * 2, (uint64_t)Lq * Hq * d * 2};
+    if (!make_map(&p.tm_q, q, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+  }
+  {
+    const uint32_t boxr[3] = {64, 1, (uint32_t)(page_size < 128 ? page_size : 128)};
+    const uint64_t dims[3] = {(uint64_t)d, (uint64_t)Hkv, (uint64_t)num_pages * page_size};
+    const uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)Hkv * d * 2};
+    if (!make_map(&p.tm_k, k_pool, bf16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
+    if (!make_map(&p.tm_v, v_pool, bf16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
+  }
+  p.o = o;
+  p.lse = lse;
+  p.o_row = static_cast<int64_t>(Hq) * d;
+  p.o_head = d;
+  p.o_batch = static_cast<int64_t>(Lq) * Hq * d;
+  p.lse_head = Lq;
+  p.lse_batch = static_cast<int64_t>(Hq) * Lq;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lq = Lq;
+  p.Lk = max_pages * page_size;
+  p.num_m_blocks = (Lq + 255) / 256;
+  p.err = err;
+  fill_common(p, opts, d);
+  p.block_table = block_table;
+  p.seqlens_k = seqlens_k;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  const bool masked = p.win_left >= 0 || p.win_right >= 0;
+  p.num_items = p.num_m_blocks * B * Hq;
+  const int grid = p.num_items < num_sms ? p.num_items : num_sms;
+  return finish_launch(launch_prefill(p, grid, d, bf16, masked, score_xf(p), stream, g_last_name,
+                                      sizeof(g_last_name)));
+}
+}  // namespace
+
+extern "C" {
+
 size_t attn_paged_workspace_bytes(int B, int Lq, int Hq, int d, int num_splits) {
   if (B <= 0 || Lq <= 0 || Hq <= 0 || d <= 0 || num_splits <= 1) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * Lq;
@@ -500,7 +573,6 @@ attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool
   if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128 &&
       page_size != 256)
     return ATTN_ERR_UNSUPPORTED;
-  if (Lq * (Hq / Hkv) > 16) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(num_pages) * page_size > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || Lq == 0) return ATTN_OK;
   if (q == nullptr || k_pool == nullptr || v_pool == nullptr || block_table == nullptr ||
@@ -514,6 +586,10 @@ attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool
     const attn_status so_ = check_opts(opts, Hq, false);
     if (so_ != ATTN_OK) return so_;
   }
+  if (static_cast<int64_t>(Lq) * (Hq / Hkv) > 16)  // a chunk of queries: prefill kernel
+    return paged_prefill(q, k_pool, v_pool, block_table, seqlens_k, o, lse, B, Lq, Hq, Hkv, d,
+                         dtype == ATTN_BF16, page_size, num_pages, max_pages_per_seq, opts,
+                         static_cast<cudaStream_t>(stream));
   const int win_pages = attn_paged_window_pages(Lq, page_size, max_pages_per_seq, opts);
   if (num_splits == 0) num_splits = attn_paged_auto_splits(B, Hkv, win_pages);
   if (num_splits > 1 && (o_partial == nullptr || lse_partial == nullptr ||

@@ -23,6 +23,7 @@ enum ErrBits : uint32_t {
   kErrPrefillPFull = 6,
   kErrPrefillOFinal = 7,
   kErrPrefillTeardown = 8,
+  kErrPrefillBadPage = 9,
   kErrDecodeFull = 12,
   kErrDecodeEmpty = 13,
   kErrDecodeBadPage = 14,
@@ -65,6 +66,12 @@ struct PrefillParams {
   int alibi_stride;
   const void* bias;                // elementwise bias (input dtype), batch mode only
   int64_t bias_row, bias_head, bias_batch;  // its element strides (key stride 1)
+  // Paged KV cache (chunked prefill): tm_k / tm_v are then 3-D maps
+  // (d, Hkv, num_pages * page_size) over the pools, and sequence b has
+  // seqlens_k[b] keys; nullptr otherwise.
+  const int32_t* block_table;
+  const int32_t* seqlens_k;
+  int page_size, max_pages, num_pages;
   unsigned int* err;
   uint64_t timeout_ns;
 };

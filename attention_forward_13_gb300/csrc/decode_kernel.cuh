@@ -1,5 +1,6 @@
-// decode.cu -- paged-KV split-KV attention forward (decode and short query
-// chunks) on sm_103a.
+// decode_kernel.cuh -- paged-KV split-KV attention forward (decode and short query
+// chunks) on sm_103a, compiled once per head dimension (decode_d64.cu,
+// decode_d128.cu define ATTN_DECODE_D and include this).
 //
 // Prior art on the pages: the Composable Kernel fmha_fwd_pagedkv_kernel.hpp
 // page block navigator (physical page = block_table[b][logical page], page
@@ -22,6 +23,7 @@
 //    (warp butterfly + 4-way shared-memory exchange); row sums stay
 //    per-thread until the end of the split.  O is rescaled only when a row
 //    max grows by more than 8 (log2 units), as in the prefill kernel.
+#pragma once
 #include "ptx.cuh"
 #include "common.cuh"
 #include "launch.h"
@@ -118,7 +120,10 @@ __device__ __forceinline__ int butterfly16_row(int lane) {
          ((lane >> 1) & 1);
 }
 
-template <int D, bool BF16, bool SOFTCAP>
+// FEAT: 0 = no mask and no ALiBi (the decode fast path), 1 = causal / window
+// masks (either alignment), 2 = masks and ALiBi.  Only the instantiations a
+// call needs pay for the per-key checks.
+template <int D, bool BF16, bool SOFTCAP, int FEAT>
 __global__ void __launch_bounds__(192, 2)
     attn_decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<D>;
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(192, 2)
   // every row's right bound reaches the last key, the first row's left bound
   // is the lowest.
   const int diag0 = p.top_left ? 0 : L - p.Lq;  // key on query row 0's diagonal
-  const int k_lo = p.win_left >= 0 ? max(0, diag0 - p.win_left) : 0;
+  const int k_lo = (FEAT > 0 && p.win_left >= 0) ? max(0, diag0 - p.win_left) : 0;
   const int pg0 = k_lo / P + split * p.chunk_pages;
   const int pg1 = min(pg0 + p.chunk_pages, pages_b);
   const int k0 = pg0 * P;
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
     for (int r = 0; r < C::NR; ++r) {
       const int h = hk * g + (r % g);
-      al[r] = (p.alibi != nullptr && r < R) ? p.alibi[b * p.alibi_stride + h] * kLog2e : 0.0f;
+      al[r] = (FEAT == 2 && r < R) ? p.alibi[b * p.alibi_stride + h] * kLog2e : 0.0f;
     }
     // Every thread runs every iteration and every named barrier even after a
     // timeout (waits then return at once), so the four warps never part ways
@@ -397,10 +402,13 @@ __global__ void __launch_bounds__(192, 2)
         } else {
           s *= p.scale_log2;
         }
-        if (p.alibi != nullptr) s = fmaf(-al[r], fabsf(static_cast<float>((r / g) + diag - key)), s);
+        if constexpr (FEAT == 2)
+          s = fmaf(-al[r], fabsf(static_cast<float>((r / g) + diag - key)), s);
         bool valid = (key < k1) && (r < R);
-        if (p.win_right >= 0) valid = valid && (key <= (r / g) + diag + p.win_right);
-        if (p.win_left >= 0) valid = valid && (key >= (r / g) + diag - p.win_left);
+        if constexpr (FEAT > 0) {
+          if (p.win_right >= 0) valid = valid && (key <= (r / g) + diag + p.win_right);
+          if (p.win_left >= 0) valid = valid && (key >= (r / g) + diag - p.win_left);
+        }
         x[r] = valid ? s : -INFINITY;
       }
       const float wmax = butterfly16<true>(x);
@@ -530,10 +538,10 @@ __global__ void __launch_bounds__(192, 2)
   }
 }
 
-template <int D, bool BF16, bool SOFTCAP>
+template <int D, bool BF16, bool SOFTCAP, int FEAT>
 static cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   using C = DecodeCfg<D>;
-  auto kern = attn_decode_kernel<D, BF16, SOFTCAP>;
+  auto kern = attn_decode_kernel<D, BF16, SOFTCAP, FEAT>;
   const int smem = static_cast<int>(sizeof(DecodeSmem<C>)) + 1024;
   static bool configured = false;
   if (!configured) {
@@ -546,22 +554,25 @@ static cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int d, bool bf16, bool softcap, int rows,
-                          cudaStream_t stream, char* name, size_t name_len) {
-  snprintf(name, name_len, "attn_decode_paged_tcgen05_d%d_%s_%s_rows%d_splits%d", d,
-           bf16 ? "bf16" : "f16", softcap ? "softcap" : "nocap", rows, p.num_splits);
-#define ATTN_DECODE_CASE(D_, B_, S_) \
-  if (d == D_ && bf16 == B_ && softcap == S_) return launch_decode_t<D_, B_, S_>(p, stream);
-  ATTN_DECODE_CASE(64, true, false)
-  ATTN_DECODE_CASE(64, true, true)
-  ATTN_DECODE_CASE(64, false, false)
-  ATTN_DECODE_CASE(64, false, true)
-  ATTN_DECODE_CASE(128, true, false)
-  ATTN_DECODE_CASE(128, true, true)
-  ATTN_DECODE_CASE(128, false, false)
-  ATTN_DECODE_CASE(128, false, true)
-#undef ATTN_DECODE_CASE
+template <bool BF16>
+static cudaError_t launch_decode_f(const DecodeParams& p, bool softcap, int feat,
+                                   cudaStream_t stream) {
+  if (softcap) {  // ALiBi with the soft-cap is rejected before launch
+    if (feat == 0) return launch_decode_t<ATTN_DECODE_D, BF16, true, 0>(p, stream);
+    if (feat == 1) return launch_decode_t<ATTN_DECODE_D, BF16, true, 1>(p, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (feat == 0) return launch_decode_t<ATTN_DECODE_D, BF16, false, 0>(p, stream);
+  if (feat == 1) return launch_decode_t<ATTN_DECODE_D, BF16, false, 1>(p, stream);
+  if (feat == 2) return launch_decode_t<ATTN_DECODE_D, BF16, false, 2>(p, stream);
   return cudaErrorInvalidValue;
+}
+
+template <>
+cudaError_t launch_decode_d<ATTN_DECODE_D>(const DecodeParams& p, bool bf16, bool softcap,
+                                           int feat, cudaStream_t stream) {
+  return bf16 ? launch_decode_f<true>(p, softcap, feat, stream)
+              : launch_decode_f<false>(p, softcap, feat, stream);
 }
 
 }  // namespace attn

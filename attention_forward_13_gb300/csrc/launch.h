@@ -19,6 +19,11 @@ cudaError_t launch_prefill_d(const PrefillParams& p, int grid, bool bf16, bool m
 
 cudaError_t launch_decode(const DecodeParams& p, int d, bool bf16, bool softcap, int rows,
                           cudaStream_t stream, char* name, size_t name_len);
+// feat: 0 none, 1 masks, 2 masks + ALiBi.  One per head dimension
+// (decode_d64.cu, decode_d128.cu).
+template <int D>
+cudaError_t launch_decode_d(const DecodeParams& p, bool bf16, bool softcap, int feat,
+                            cudaStream_t stream);
 
 cudaError_t launch_combine(const CombineParams& p, bool bf16, cudaStream_t stream, char* name,
                            size_t name_len);

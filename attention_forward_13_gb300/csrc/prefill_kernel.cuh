@@ -183,6 +183,39 @@ struct PrefillItem {
   int ue[2];
 };
 
+// One 128-key K or V tile of sequence it.b gathered from a paged pool
+// (Composable Kernel page block navigator: key j is row j mod page of
+// physical page block_table[b][j / page]).  The map is 3-D (d, Hkv, pool
+// rows); one box of min(page, 128) rows per page piece and 64-column chunk.
+// Pieces past the sequence end, or behind a block-table entry outside
+// [0, num_pages) (an error: device error word bit), load from one row past
+// the pool, which the copy engine fills with zeros, so every tile delivers
+// its full byte count.
+template <class C>
+__device__ __forceinline__ void load_paged_tile(const PrefillParams& p, const PrefillItem& it,
+                                                int key0, const CUtensorMap* map, uint8_t* dst,
+                                                uint64_t* bar) {
+  const int P = p.page_size;
+  const int BR = P < C::BN ? P : C::BN;  // rows per box
+  const int32_t* bt = p.block_table + static_cast<int64_t>(it.b) * p.max_pages;
+  const int oob_row = p.num_pages * P;
+  for (int r0 = 0; r0 < C::BN; r0 += BR) {
+    const int key = key0 + r0;
+    int row = oob_row;
+    if (key < it.Lk) {
+      const int lp = key / P;
+      const int phys = lp < p.max_pages ? bt[lp] : -1;
+      if (phys >= 0 && phys < p.num_pages)
+        row = phys * P + (key - lp * P);
+      else if (p.err)
+        atomicOr(p.err, 1u << kErrPrefillBadPage);
+    }
+#pragma unroll
+    for (int c = 0; c < C::NCHUNK; ++c)
+      tma_load_3d(dst + c * C::CHUNK_BYTES + r0 * 128, map, bar, c * 64, it.hk, row);
+  }
+}
+
 // Item index -> coordinates.  Masked problems list the heaviest query blocks
 // first (Composable Kernel GetTileIndex reverses the m-tile order when
 // masking).  Returns false when the block starts past the sequence end.
@@ -214,6 +247,8 @@ __device__ __forceinline__ bool decode_item(const PrefillParams& p, int item, Pr
     it.Lq = min(it.Lq, p.total_q - it.rq0);
     if (it.rk0 < 0 || it.rk0 > p.total_k) it.Lk = 0;
     it.Lk = max(0, min(it.Lk, p.total_k - it.rk0));
+  } else if (p.seqlens_k != nullptr) {  // paged KV cache: per-sequence key count
+    it.Lk = max(0, min(p.seqlens_k[it.b], p.max_pages * p.page_size));
   }
   it.m0 = mb * 2 * BM;
   if (it.m0 >= it.Lq) return false;
@@ -325,17 +360,25 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           const uint32_t ph = (g / C::NS) & 1;
           if (!(ok = w.wait(&sm.k_empty[s], ph ^ 1, kErrPrefillKEmpty))) break;
           mbar_arrive_expect_tx(&sm.k_full[s], C::TILE_BYTES);
+          if (p.block_table != nullptr) {
+            load_paged_tile<C>(p, it, (it.jb + j) * C::BN, &p.tm_k, sm.k[s], &sm.k_full[s]);
+          } else {
 #pragma unroll
-          for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_4d(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s], c * 64,
-                        it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
+            for (int c = 0; c < C::NCHUNK; ++c)
+              tma_load_4d(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s], c * 64,
+                          it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
+          }
           ++k_armed;
           if (!(ok = w.wait(&sm.v_empty[s], ph ^ 1, kErrPrefillVEmpty))) break;
           mbar_arrive_expect_tx(&sm.v_full[s], C::TILE_BYTES);
+          if (p.block_table != nullptr) {
+            load_paged_tile<C>(p, it, (it.jb + j) * C::BN, &p.tm_v, sm.v[s], &sm.v_full[s]);
+          } else {
 #pragma unroll
-          for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_4d(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s], c * 64,
-                        it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
+            for (int c = 0; c < C::NCHUNK; ++c)
+              tma_load_4d(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s], c * 64,
+                          it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
+          }
           ++v_armed;
         }
       }

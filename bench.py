@@ -88,6 +88,17 @@ def dense_flops(B, Hq, Lq, Lk, d, causal):
     return 4.0 * d * B * Hq * pairs
 
 
+def window_pairs(Lq, Lk, left, right):
+    """Kept (i, j) pairs of a bottom-right band left/right (negative = unbounded)."""
+    n = 0
+    for i in range(Lq):
+        dg = i + Lk - Lq
+        lo = 0 if left < 0 else max(0, dg - left)
+        hi = Lk - 1 if right < 0 else min(Lk - 1, dg + right)
+        n += max(0, hi - lo + 1)
+    return n
+
+
 def varlen_flops(lens, Hq, d, causal):
     return sum(4.0 * d * Hq * (causal_pairs(L, L) if causal else L * L) for L in lens)
 
@@ -334,6 +345,69 @@ def run_extra(args, rank, pk, stream, flush, only=None):
         out.update(_extra_decode(A, inputs, pk, stream, flush, steps, warm, args.decode_batch))
     if only in (None, "varlen"):
         out.update(_extra_varlen(A, inputs, pk, stream, flush, steps, warm))
+    if only in (None, "masks"):
+        out.update(_extra_masks(A, inputs, pk, stream, flush, steps, warm))
+    if only in (None, "chunked"):
+        out.update(_extra_chunked(A, inputs, pk, stream, flush, steps, warm))
+    return out
+
+
+def _extra_chunked(A, inputs, pk, stream, flush, steps, warm):
+    """Chunked prefill over a paged cache: 8 sequences of U[2048, 8192] cached
+    keys (the chunk's own 512 included), Hq 32 / Hkv 8, d 128, page 64, causal."""
+    lens = inputs.random_lengths(8, 2048, 8192, seed=1010)
+    Lq, Hq, Hkv, d, page = 512, 32, 8, 128, 64
+    npages = sum((L + page - 1) // page for L in lens) + 16
+    inp = inputs.paged(lens, Lq, Hq, Hkv, d, page, npages, seed=1010, device="cuda", causal=True)
+    bt, sl = inp.block_table.cuda(), inp.seqlens_k.cuda()
+    fl = sum(4.0 * d * Hq * causal_pairs(Lq, L) for L in lens)
+    t = time_steps(lambda: A.attn_fwd_paged(inp.q, inp.k_pool, inp.v_pool, bt, sl, causal=True),
+                   steps, warm, stream, flush)
+    return {"chunked_prefill_paged_B8_chunk512_Hq32_Hkv8_d128_page64": _tensor_entry(
+        fl, statistics.mean(t), pk, A.attn_last_kernel_name())}
+
+
+def _tensor_entry(fl, ms, pk, kernel, **extra):
+    tf = fl / (ms * 1e-3) / 1e12
+    e = {"value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "kernel": kernel,
+         "roofline": {"bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                      "frac": round(tf / pk["bf16_tflops"], 4)}}
+    e.update(extra)
+    return e
+
+
+def _extra_masks(A, inputs, pk, stream, flush, steps, warm):
+    """The sliding-window, ALiBi and elementwise-bias variants on the headline
+    shape (FLOPs count kept pairs only)."""
+    import torch
+    out = {}
+    B, H, L, d = 4, 16, 2048, 128
+    inp = inputs.dense(B, H, H, L, L, d, "bf16", seed=1002, device="cuda", causal=True)
+    o = torch.empty_like(inp.q)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    fl = 4.0 * d * B * H * window_pairs(L, L, 512, 0)
+    t = time_steps(lambda: A.attn_fwd(inp.q, inp.k, inp.v, o=o, lse=lse, causal=True,
+                                      window=(512, -1)), steps, warm, stream, flush)
+    out["window512_causal_prefill_B4_H16_L2048_d128"] = _tensor_entry(
+        fl, statistics.mean(t), pk, A.attn_last_kernel_name())
+    slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], device="cuda")
+    fl = dense_flops(B, H, L, L, d, True)
+    t = time_steps(lambda: A.attn_fwd(inp.q, inp.k, inp.v, o=o, lse=lse, causal=True,
+                                      alibi_slopes=slopes), steps, warm, stream, flush)
+    out["alibi_causal_prefill_B4_H16_L2048_d128"] = _tensor_entry(
+        fl, statistics.mean(t), pk, A.attn_last_kernel_name())
+    # One bias per head (bf16 [1,H,L,L], 128 MiB read once per call).
+    g = torch.Generator(device="cuda").manual_seed(1009)
+    bias = torch.randn((1, H, L, L), generator=g, device="cuda").to(torch.bfloat16)
+    q1, k1, v1 = inp.q[:1], inp.k[:1], inp.v[:1]
+    o1, l1 = o[:1], lse[:1]
+    fl = dense_flops(1, H, L, L, d, False)
+    t = time_steps(lambda: A.attn_fwd(q1, k1, v1, o=o1, lse=l1, bias=bias), steps, warm,
+                   stream, flush)
+    ms = statistics.mean(t)
+    out["bias_prefill_B1_H16_L2048_d128"] = _tensor_entry(
+        fl, ms, pk, A.attn_last_kernel_name(),
+        bias_gbs=round(bias.numel() * 2 / (ms * 1e-3) / 1e9, 1))
     return out
 
 
@@ -476,7 +550,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["gqa", "decode", "varlen"], default=None,
+    ap.add_argument("--only", choices=["gqa", "decode", "varlen", "masks", "chunked"],
+                    default=None,
                     help="run one secondary workload alone (profiling) and print its line")
     ap.add_argument("--decode-batch", type=int, default=64)
     args = ap.parse_args()

@@ -143,8 +143,13 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
  *   (device error word bit, that page's keys skipped).
  *   o [B][Lq][Hq][d] contiguous (input dtype); lse fp32 [B][Hq][Lq] or NULL.
  *   Causal masking, if set, is bottom-right within each sequence.
- *   Requires Lq * (Hq / Hkv) <= 16 (decode and short chunks), page_size a
- *   multiple of 16 and <= 256.
+ *   page_size one of 16, 32, 64, 128, 256.
+ *   Lq * (Hq / Hkv) <= 16 (decode, short chunks) runs the split-KV decode
+ *   kernel described below.  Longer chunks (chunked prefill: the chunk's
+ *   own keys already written to the cache, L_b counting them) run the
+ *   prefill kernel with its K/V tiles gathered page by page; there
+ *   num_splits, o_partial and lse_partial are ignored and nothing else
+ *   changes.
  *   num_splits: 0 = choose automatically (attn_paged_auto_splits), else
  *   1..64.  Split s of sequence b covers logical pages
  *   [f_b + s*c, min(f_b + (s+1)*c, e_b)), c = ceil(W / num_splits); a split

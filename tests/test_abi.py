@@ -112,7 +112,7 @@ def test_paged_validation():
                                   a["splits"], None, None, ctypes.byref(opts), None)
 
     assert call(page=48) == 2       # page size must be a power of two in [16, 256]
-    assert call(Lq=5) == 2          # Lq * g = 20 > 16 rows
+    assert call(Lq=5, d=96) == 2    # head dim (Lq * g > 16 routes to the prefill kernel)
     assert call(splits=65) == 1
     assert call(splits=3) == 1      # splits > 1 needs the scratch buffers
     assert call(num_pages=0) == 1
