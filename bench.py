@@ -51,7 +51,8 @@ def peaks():
 def kernel_source_sha(name: str) -> str:
     path = os.path.join(ROOT, "attention_forward_13_gb300", "csrc", name)
     h = hashlib.sha256()
-    for f in (path, os.path.join(os.path.dirname(path), "ptx.cuh")):
+    for f in (path, os.path.join(os.path.dirname(path), "ptx.cuh"),
+              os.path.join(os.path.dirname(path), "common.cuh")):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -309,7 +310,7 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "tensor", "achieved": round(kern_tflops, 2),
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(kern_tflops / pk["bf16_tflops"], 4),
-                     "traffic": traffic_for("prefill_B4H16L2048d128_causal", "prefill.cu"),
+                     "traffic": traffic_for("prefill_B4H16L2048d128_causal", "prefill_kernel.cuh"),
                      "peak_source": f"{pk_src} bf16 burst (MEASURED_PEAKS.json)"
                      if pk_src == "measured" else "fallback 1.9 PFLOP/s",
                      "kernel": A.attn_last_kernel_name(),
