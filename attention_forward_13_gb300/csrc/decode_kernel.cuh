@@ -454,10 +454,16 @@ __global__ void __launch_bounds__(192, 2)
         }
       }
       fence_proxy_async_smem();
-      // O rescale needs the previous P.V to be complete.
-      if (ok && any_rescale && i > 0) {
+      // Wait for P.V(i-1) at every step (phase i-1 of o_done; P.V(i-2) is
+      // done, the S commit seen above covers it, so the parity is exact):
+      // an O rescale needs it, and waiting for each phase in turn keeps the
+      // final wait of the epilogue exact as well (o_done completes once per
+      // P.V; a parity wait cannot tell phases two apart).
+      if (ok && i > 0) {
         const bool got = __all_sync(0xffffffffu, w.wait(&sm.o_done, (i - 1) & 1, kErrDecodeFull));
-        if (got) {
+        if (!got) {
+          ok = false;
+        } else if (any_rescale) {
           tc_fence_after();
           uint32_t ov[16];
           tmem_ld16(tmem + C::TM_O + lane_base, ov);
@@ -468,8 +474,6 @@ __global__ void __launch_bounds__(192, 2)
             ov[r] = __float_as_uint(__uint_as_float(ov[r]) * alpha[r]);
           tmem_st16(tmem + C::TM_O + lane_base, ov);
           tmem_st_wait();
-        } else {
-          ok = false;
         }
       }
       tc_fence_before();
@@ -483,6 +487,8 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
     for (int r = 0; r < C::NR; ++r)
       l[r] = (sm.lred[0][r] + sm.lred[1][r]) + (sm.lred[2][r] + sm.lred[3][r]);
+    // Every step i >= 1 waited for P.V(i-1) (phase i-1 of o_done), so the
+    // barrier is now in phase nblk-1 or nblk and this parity wait is exact.
     const bool have_o =
         __all_sync(0xffffffffu, ok && w.wait(&sm.o_done, (nblk - 1) & 1, kErrDecodeFull));
     if (have_o) {

@@ -138,6 +138,29 @@ def test_workload4_full_size_sampled():
     no_device_error()
 
 
+def test_split_results_are_repeatable_and_match_one_split():
+    """The split-KV path is deterministic (fixed reduction orders), so three
+    runs agree bit for bit, and with 4 or 8 splits it agrees with the single
+    split within two bf16 steps at |O| < 1 (0.01): a lost or duplicated P.V
+    contribution, as from a partial O read before its last P.V completes,
+    shows up far above that."""
+    inp = inputs.workload(4, device="cuda")
+    bt, sl = inp.block_table.cuda(), inp.seqlens_k.cuda()
+    o1, l1 = A.attn_fwd_paged(inp.q, inp.k_pool, inp.v_pool, bt, sl, num_splits=1)
+    outs = []
+    for splits in (4, 4, 4, 8):
+        o, lse = A.attn_fwd_paged(inp.q, inp.k_pool, inp.v_pool, bt, sl, num_splits=splits)
+        torch.cuda.synchronize()
+        outs.append((splits, o.clone(), lse.clone()))
+    for _, o, lse in outs[1:3]:
+        assert torch.equal(o, outs[0][1]) and torch.equal(lse, outs[0][2])
+    for splits, o, lse in outs:
+        err = (o.float() - o1.float()).abs().max().item()
+        assert err <= 0.01, (splits, err)
+        assert (lse - l1).abs().max().item() <= 1e-4
+    no_device_error()
+
+
 def test_timeout_path_reports_and_recovers():
     """A kernel whose wait can never complete gives up after its limit, sets
     the error word and returns; the context stays usable."""
