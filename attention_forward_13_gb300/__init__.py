@@ -45,6 +45,8 @@ def _dtype_code(t: torch.Tensor) -> int:
         return _lib.ATTN_BF16
     if t.dtype == torch.float16:
         return _lib.ATTN_F16
+    if t.dtype == torch.float8_e4m3fn:
+        return _lib.ATTN_E4M3
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
@@ -57,7 +59,8 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _opts(scale, causal, softcap, sink, window=None, top_left=False, alibi=None, bias=None):
+def _opts(scale, causal, softcap, sink, window=None, top_left=False, alibi=None, bias=None,
+          scale_p=None, scale_o=None):
     o = _lib.attn_opts()
     o.scale = float(scale) if scale is not None else 0.0
     o.causal = 1 if causal else 0
@@ -73,6 +76,8 @@ def _opts(scale, causal, softcap, sink, window=None, top_left=False, alibi=None,
     if bias is not None:
         o.bias = bias.data_ptr()
         o.bias_strides = _lib.attn_strides(*_bias_strides(bias))
+    o.scale_p = float(scale_p) if scale_p else 0.0
+    o.scale_o = float(scale_o) if scale_o else 0.0
     return o
 
 
@@ -118,12 +123,15 @@ def _check_sink(sink, Hq, device):
 
 
 def attn_fwd(q, k, v, o=None, lse=True, causal=False, scale=None, softcap=0.0, sink=None,
-             stream=None, window=None, top_left=False, alibi_slopes=None, bias=None):
+             stream=None, window=None, top_left=False, alibi_slopes=None, bias=None,
+             scale_p=None, scale_o=None):
     """Dense attention.  q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] (any strides with d-stride 1).
     ``window`` = (left, right) keeps keys i+Lk-Lq-left <= j <= i+Lk-Lq+right (a
     negative side is unbounded); ``top_left`` drops the Lk-Lq shift.
     ``alibi_slopes``: fp32 [Hq] or [B,Hq]; ``bias``: [B|1,Hq|1,Lq,Lk] in the input
-    dtype, added to the scaled score.  Returns (o [B,Hq,Lq,d], lse fp32 [B,Hq,Lq] or None)."""
+    dtype, added to the scaled score.  float8_e4m3fn inputs (d = 128) run the FP8 path: O is
+    e4m3, scale_o * scale_p * softmax(S) V saturated.  Returns (o [B,Hq,Lq,d], lse fp32
+    [B,Hq,Lq] or None)."""
     B, Hq, Lq, d = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     if o is None:
@@ -137,7 +145,8 @@ def attn_fwd(q, k, v, o=None, lse=True, causal=False, scale=None, softcap=0.0, s
     alibi_slopes = _check_alibi(alibi_slopes, B, Hq, q.device)
     if bias is not None and (bias.dtype != q.dtype or bias.device != q.device):
         raise ValueError("bias must have the input dtype and device")
-    opts = _opts(scale, causal, softcap, sink, window, top_left, alibi_slopes, bias)
+    opts = _opts(scale, causal, softcap, sink, window, top_left, alibi_slopes, bias, scale_p,
+                 scale_o)
     st = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, Hq, Hkv, Lq, Lk,
                             d, _dtype_code(q), _strides_bhld(q), _strides_bhld(k),
                             _strides_bhld(v), _strides_bhld(o), ctypes.byref(opts),
@@ -148,7 +157,7 @@ def attn_fwd(q, k, v, o=None, lse=True, causal=False, scale=None, softcap=0.0, s
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, o=None, lse=True,
                     causal=False, scale=None, softcap=0.0, sink=None, stream=None, window=None,
-                    top_left=False, alibi_slopes=None):
+                    top_left=False, alibi_slopes=None, scale_p=None, scale_o=None):
     """Group mode.  q [total_q,Hq,d], k/v [total_k,Hkv,d], cu_seqlens int32 [B+1] on the
     device.  Returns (o [total_q,Hq,d], lse fp32 [Hq,total_q] or None)."""
     total_q, Hq, d = q.shape
@@ -166,7 +175,8 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, o=None, l
         lse_t = lse
     sink = _check_sink(sink, Hq, q.device)
     alibi_slopes = _check_alibi(alibi_slopes, B, Hq, q.device)
-    opts = _opts(scale, causal, softcap, sink, window, top_left, alibi_slopes)
+    opts = _opts(scale, causal, softcap, sink, window, top_left, alibi_slopes, None, scale_p,
+                 scale_o)
     st = library().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t),
                                    _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, total_q, total_k,
                                    int(max_seqlen_q), Hq, Hkv, d, _dtype_code(q),

@@ -22,12 +22,13 @@ class attn_opts(ctypes.Structure):
                 ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
                 ("top_left", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
                 ("alibi_stride", ctypes.c_int), ("bias", ctypes.c_void_p),
-                ("bias_strides", attn_strides)]
+                ("bias_strides", attn_strides), ("scale_p", ctypes.c_float),
+                ("scale_o", ctypes.c_float)]
 
 
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
           4: "ATTN_ERR_TIMEOUT"}
-ATTN_F16, ATTN_BF16 = 0, 1
+ATTN_F16, ATTN_BF16, ATTN_E4M3 = 0, 1, 2
 
 EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_splitkv_combine",
            "attn_paged_workspace_bytes", "attn_paged_auto_splits", "attn_status_string",

@@ -80,7 +80,8 @@ EncodeTiledFn encode_fn() {
 // Tiled map over a tensor whose innermost dimension is d (contiguous) and
 // whose other dimensions have the given extents and byte strides; the box is
 // 64 elements (128 bytes, one swizzle atom) by box[1..].
-bool make_map(CUtensorMap* m, const void* base, bool bf16, int rank, const uint64_t* dims,
+// dt: attn_dtype of the elements (e4m3 travels as bytes).
+bool make_map(CUtensorMap* m, const void* base, int dt, int rank, const uint64_t* dims,
               const uint64_t* strides_bytes, const uint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
@@ -94,7 +95,10 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int rank, const uint6
     es[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+  const CUtensorMapDataType ty = dt == ATTN_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dt == ATTN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = fn(m, ty,
                   rank, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -102,7 +106,8 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int rank, const uint6
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool stride_ok(int64_t s) { return s > 0 && (s % 8) == 0; }
+// Element strides: positive and a whole number of 16-byte units.
+bool stride_ok(int64_t s, int eb = 2) { return s > 0 && (s * eb) % 16 == 0; }
 
 float resolve_scale(const attn_opts* o, int d) {
   return (o != nullptr && o->scale > 0.0f) ? o->scale : 1.0f / sqrtf(static_cast<float>(d));
@@ -131,6 +136,8 @@ void fill_common(PrefillParams& p, const attn_opts* opts, int d) {
   resolve_window(opts, &p.win_left, &p.win_right);
   p.top_left = (opts != nullptr && opts->top_left) ? 1 : 0;
   p.inv_scale = 1.0f / scale;
+  p.o_scale = ((opts != nullptr && opts->scale_p > 0.0f) ? opts->scale_p : 1.0f) *
+              ((opts != nullptr && opts->scale_o > 0.0f) ? opts->scale_o : 1.0f);
   p.alibi = opts != nullptr ? opts->alibi_slopes : nullptr;
   p.alibi_stride = opts != nullptr ? opts->alibi_stride : 0;
   p.timeout_ns = kTimeoutNs;
@@ -182,17 +189,18 @@ cudaError_t launch_decode(const DecodeParams& p, int d, bool bf16, bool softcap,
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool masked,
+cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, int dt, bool masked,
                            int xf, cudaStream_t stream, char* name, size_t name_len) {
   const char* mask = !masked ? "nomask"
                      : (p.win_left < 0 && p.win_right == 0) ? "causal"
                                                             : "window";
   static const char* const kXfName[4] = {"plain", "softcap", "alibi", "bias"};
   snprintf(name, name_len, "attn_prefill_tcgen05_d%d_%s_%s%s_%s_m256n128_persistent", d,
-           bf16 ? "bf16" : "f16", mask, p.top_left ? "_topleft" : "",
+           dt == kDtE4M3 ? "e4m3" : dt == kDtBF16 ? "bf16" : "f16", mask,
+           p.top_left ? "_topleft" : "",
            kXfName[(xf >= 0 && xf < 4) ? xf : 0]);
-  if (d == 64) return launch_prefill_d<64>(p, grid, bf16, masked, xf, stream);
-  if (d == 128) return launch_prefill_d<128>(p, grid, bf16, masked, xf, stream);
+  if (d == 64) return launch_prefill_d<64>(p, grid, dt, masked, xf, stream);
+  if (d == 128) return launch_prefill_d<128>(p, grid, dt, masked, xf, stream);
   return cudaErrorInvalidValue;
 }
 }  // namespace attn
@@ -279,8 +287,13 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      attn_strides sk, attn_strides sv, attn_strides so, const attn_opts* opts,
                      void* stream) {
   if (B < 0 || Lq < 0 || Lk < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
-  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16 && dtype != ATTN_E4M3) return ATTN_ERR_INVALID;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype == ATTN_E4M3 && (d != 128 || (opts != nullptr &&
+                                           (opts->softcap > 0.0f || opts->alibi_slopes != nullptr ||
+                                            opts->bias != nullptr))))
+    return ATTN_ERR_UNSUPPORTED;
+  const int eb = dtype == ATTN_E4M3 ? 1 : 2;  // bytes per element
   if (B == 0 || Lq == 0) return ATTN_OK;
   // With Lk = 0 nothing of K/V is read and they may be NULL.
   if (q == nullptr || o == nullptr || (Lk > 0 && (k == nullptr || v == nullptr)))
@@ -289,7 +302,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
       (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return ATTN_ERR_INVALID;
   for (const attn_strides* s : {&sq, &sk, &sv, &so})
-    if (!stride_ok(s->row) || !stride_ok(s->head) || !stride_ok(s->batch)) return ATTN_ERR_INVALID;
+    if (!stride_ok(s->row, eb) || !stride_ok(s->head, eb) || !stride_ok(s->batch, eb))
+      return ATTN_ERR_INVALID;
   {
     const attn_status so_ = check_opts(opts, Hq, true);
     if (so_ != ATTN_OK) return so_;
@@ -301,25 +315,25 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   unsigned int* err = nullptr;
   int num_sms = 0;
   if (device_state(&err, &num_sms) != ATTN_OK) return ATTN_ERR_CUDA;
-  const bool bf16 = dtype == ATTN_BF16;
-  const uint32_t box[4] = {64, 128, 1, 1};
+  const int dt = dtype == ATTN_E4M3 ? kDtE4M3 : dtype == ATTN_BF16 ? kDtBF16 : kDtF16;
+  const uint32_t box[4] = {(uint32_t)(128 / eb), 128, 1, 1};
   {
     const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lq, (uint64_t)Hq, (uint64_t)B};
-    const uint64_t st[3] = {(uint64_t)sq.row * 2, (uint64_t)sq.head * 2, (uint64_t)sq.batch * 2};
-    if (!make_map(&p.tm_q, q, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+    const uint64_t st[3] = {(uint64_t)sq.row * eb, (uint64_t)sq.head * eb, (uint64_t)sq.batch * eb};
+    if (!make_map(&p.tm_q, q, dtype, 4, dims, st, box)) return ATTN_ERR_INVALID;
   }
   if (Lk > 0) {  // Lk = 0: no key tile is ever loaded, the maps stay unused
     {
       const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lk, (uint64_t)Hkv, (uint64_t)B};
-      const uint64_t st[3] = {(uint64_t)sk.row * 2, (uint64_t)sk.head * 2,
-                              (uint64_t)sk.batch * 2};
-      if (!make_map(&p.tm_k, k, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+      const uint64_t st[3] = {(uint64_t)sk.row * eb, (uint64_t)sk.head * eb,
+                              (uint64_t)sk.batch * eb};
+      if (!make_map(&p.tm_k, k, dtype, 4, dims, st, box)) return ATTN_ERR_INVALID;
     }
     {
       const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lk, (uint64_t)Hkv, (uint64_t)B};
-      const uint64_t st[3] = {(uint64_t)sv.row * 2, (uint64_t)sv.head * 2,
-                              (uint64_t)sv.batch * 2};
-      if (!make_map(&p.tm_v, v, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+      const uint64_t st[3] = {(uint64_t)sv.row * eb, (uint64_t)sv.head * eb,
+                              (uint64_t)sv.batch * eb};
+      if (!make_map(&p.tm_v, v, dtype, 4, dims, st, box)) return ATTN_ERR_INVALID;
     }
   }
   p.o = o;
@@ -347,7 +361,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
   p.num_items = p.num_m_blocks * B * Hq;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
-  return finish_launch(launch_prefill(p, grid, d, bf16, masked, score_xf(p),
+  return finish_launch(launch_prefill(p, grid, d, dt, masked, score_xf(p),
                                       static_cast<cudaStream_t>(stream), g_last_name,
                                       sizeof(g_last_name)));
 }
@@ -360,8 +374,13 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   if (B < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || Hq <= 0 || Hkv <= 0 ||
       Hq % Hkv != 0)
     return ATTN_ERR_INVALID;
-  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16 && dtype != ATTN_E4M3) return ATTN_ERR_INVALID;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype == ATTN_E4M3 && (d != 128 || (opts != nullptr &&
+                                           (opts->softcap > 0.0f || opts->alibi_slopes != nullptr ||
+                                            opts->bias != nullptr))))
+    return ATTN_ERR_UNSUPPORTED;
+  const int eb = dtype == ATTN_E4M3 ? 1 : 2;  // bytes per element
   if (B == 0 || total_q == 0 || max_seqlen_q == 0) return ATTN_OK;
   if (q == nullptr || o == nullptr || cu_seqlens_q == nullptr || cu_seqlens_k == nullptr ||
       (total_k > 0 && (k == nullptr || v == nullptr)))
@@ -370,7 +389,7 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
       (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return ATTN_ERR_INVALID;
   for (const attn_strides* s : {&sq, &sk, &sv, &so})
-    if (!stride_ok(s->row) || !stride_ok(s->head)) return ATTN_ERR_INVALID;
+    if (!stride_ok(s->row, eb) || !stride_ok(s->head, eb)) return ATTN_ERR_INVALID;
   if (static_cast<int64_t>(B) * Hq * ((max_seqlen_q + 255) / 256) > 0x7fffffffLL)
     return ATTN_ERR_UNSUPPORTED;
   {
@@ -383,27 +402,27 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   unsigned int* err = nullptr;
   int num_sms = 0;
   if (device_state(&err, &num_sms) != ATTN_OK) return ATTN_ERR_CUDA;
-  const bool bf16 = dtype == ATTN_BF16;
-  const uint32_t box[4] = {64, 128, 1, 1};
+  const int dt = dtype == ATTN_E4M3 ? kDtE4M3 : dtype == ATTN_BF16 ? kDtBF16 : kDtF16;
+  const uint32_t box[4] = {(uint32_t)(128 / eb), 128, 1, 1};
   {
     const uint64_t dims[4] = {(uint64_t)d, (uint64_t)total_q, (uint64_t)Hq, 1};
-    const uint64_t st[3] = {(uint64_t)sq.row * 2, (uint64_t)sq.head * 2,
-                            (uint64_t)sq.row * 2 * (uint64_t)total_q};
-    if (!make_map(&p.tm_q, q, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+    const uint64_t st[3] = {(uint64_t)sq.row * eb, (uint64_t)sq.head * eb,
+                            (uint64_t)sq.row * eb * (uint64_t)total_q};
+    if (!make_map(&p.tm_q, q, dtype, 4, dims, st, box)) return ATTN_ERR_INVALID;
   }
   if (total_k > 0) {  // no keys at all: the maps stay unused
     const int tk = total_k;
     {
       const uint64_t dims[4] = {(uint64_t)d, (uint64_t)tk, (uint64_t)Hkv, 1};
-      const uint64_t st[3] = {(uint64_t)sk.row * 2, (uint64_t)sk.head * 2,
-                              (uint64_t)sk.row * 2 * (uint64_t)tk};
-      if (!make_map(&p.tm_k, k, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+      const uint64_t st[3] = {(uint64_t)sk.row * eb, (uint64_t)sk.head * eb,
+                              (uint64_t)sk.row * eb * (uint64_t)tk};
+      if (!make_map(&p.tm_k, k, dtype, 4, dims, st, box)) return ATTN_ERR_INVALID;
     }
     {
       const uint64_t dims[4] = {(uint64_t)d, (uint64_t)tk, (uint64_t)Hkv, 1};
-      const uint64_t st[3] = {(uint64_t)sv.row * 2, (uint64_t)sv.head * 2,
-                              (uint64_t)sv.row * 2 * (uint64_t)tk};
-      if (!make_map(&p.tm_v, v, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+      const uint64_t st[3] = {(uint64_t)sv.row * eb, (uint64_t)sv.head * eb,
+                              (uint64_t)sv.row * eb * (uint64_t)tk};
+      if (!make_map(&p.tm_v, v, dtype, 4, dims, st, box)) return ATTN_ERR_INVALID;
     }
   }
   p.o = o;
@@ -428,7 +447,7 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
   p.num_items = p.num_m_blocks * B * Hq;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
-  return finish_launch(launch_prefill(p, grid, d, bf16, masked, score_xf(p),
+  return finish_launch(launch_prefill(p, grid, d, dt, masked, score_xf(p),
                                       static_cast<cudaStream_t>(stream), g_last_name,
                                       sizeof(g_last_name)));
 }
@@ -455,14 +474,14 @@ attn_status paged_prefill(const void* q, const void* k_pool, const void* v_pool,
     const uint32_t box[4] = {64, 128, 1, 1};
     const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lq, (uint64_t)Hq, (uint64_t)B};
     const uint64_t st[3] = {(uint64_t)Hq * d * 2, (uint64_t)d * 2, (uint64_t)Lq * Hq * d * 2};
-    if (!make_map(&p.tm_q, q, bf16, 4, dims, st, box)) return ATTN_ERR_INVALID;
+    if (!make_map(&p.tm_q, q, bf16 ? ATTN_BF16 : ATTN_F16, 4, dims, st, box)) return ATTN_ERR_INVALID;
   }
   {
     const uint32_t boxr[3] = {64, 1, (uint32_t)(page_size < 128 ? page_size : 128)};
     const uint64_t dims[3] = {(uint64_t)d, (uint64_t)Hkv, (uint64_t)num_pages * page_size};
     const uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)Hkv * d * 2};
-    if (!make_map(&p.tm_k, k_pool, bf16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
-    if (!make_map(&p.tm_v, v_pool, bf16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
+    if (!make_map(&p.tm_k, k_pool, bf16 ? ATTN_BF16 : ATTN_F16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
+    if (!make_map(&p.tm_v, v_pool, bf16 ? ATTN_BF16 : ATTN_F16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
   }
   p.o = o;
   p.lse = lse;
@@ -487,7 +506,7 @@ attn_status paged_prefill(const void* q, const void* k_pool, const void* v_pool,
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
   p.num_items = p.num_m_blocks * B * Hq;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;
-  return finish_launch(launch_prefill(p, grid, d, bf16, masked, score_xf(p), stream, g_last_name,
+  return finish_launch(launch_prefill(p, grid, d, bf16 ? kDtBF16 : kDtF16, masked, score_xf(p), stream, g_last_name,
                                       sizeof(g_last_name)));
 }
 }  // namespace
@@ -606,8 +625,8 @@ attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool
   (void)box;
   const uint64_t dims[3] = {(uint64_t)d, (uint64_t)Hkv, (uint64_t)num_pages * page_size};
   const uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)Hkv * d * 2};
-  if (!make_map(&p.tm_k, k_pool, bf16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
-  if (!make_map(&p.tm_v, v_pool, bf16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
+  if (!make_map(&p.tm_k, k_pool, bf16 ? ATTN_BF16 : ATTN_F16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
+  if (!make_map(&p.tm_v, v_pool, bf16 ? ATTN_BF16 : ATTN_F16, 3, dims, st, boxr)) return ATTN_ERR_INVALID;
   p.q = q;
   p.block_table = block_table;
   p.seqlens_k = seqlens_k;

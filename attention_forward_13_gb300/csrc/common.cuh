@@ -31,6 +31,11 @@ enum ErrBits : uint32_t {
   kErrSelftest = 20,
 };
 
+// Element types of a prefill instantiation: fp16 / bf16 end to end, or e4m3
+// Q/K/V/O (FP8 static quantisation: S on the kind::f8f6f4 tensor path, V
+// widened to fp16 on chip for P.V, O scaled and saturated to e4m3).
+enum PrefillDt : int { kDtF16 = 0, kDtBF16 = 1, kDtE4M3 = 2 };
+
 // Score transform of a prefill instantiation (applied to the raw score
 // before masking).
 enum ScoreXf : int { kXfNone = 0, kXfSoftcap = 1, kXfAlibi = 2, kXfBias = 3 };
@@ -61,6 +66,7 @@ struct PrefillParams {
   // masking is win_right = 0.  Only read by the masked instantiations.
   int win_left, win_right;
   int top_left;                    // masks and ALiBi aligned top-left (row i on key i)
+  float o_scale;                   // FP8 static quantisation: scale_p * scale_o on O
   float inv_scale;                 // 1 / scale (bias and ALiBi go to raw-score units)
   const float* alibi;              // ALiBi slopes, (b, h) at b * alibi_stride + h
   int alibi_stride;

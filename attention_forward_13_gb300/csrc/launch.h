@@ -9,12 +9,13 @@ namespace attn {
 
 // grid = number of CTAs; name receives the kernel's trait string.  xf is a
 // ScoreXf value.  Dispatches to launch_prefill_d<64 / 128>.
-cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, bool bf16, bool masked,
+cudaError_t launch_prefill(const PrefillParams& p, int grid, int d, int dt, bool masked,
                            int xf, cudaStream_t stream, char* name, size_t name_len);
 // One per head dimension, each in its own translation unit (prefill_d64.cu,
 // prefill_d128.cu) so the two compile in parallel.
+// dt: PrefillDt (0 fp16, 1 bf16, 2 e4m3).
 template <int D>
-cudaError_t launch_prefill_d(const PrefillParams& p, int grid, bool bf16, bool masked, int xf,
+cudaError_t launch_prefill_d(const PrefillParams& p, int grid, int dt, bool masked, int xf,
                              cudaStream_t stream);
 
 cudaError_t launch_decode(const DecodeParams& p, int d, bool bf16, bool softcap, int rows,

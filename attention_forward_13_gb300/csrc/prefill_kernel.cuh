@@ -42,15 +42,21 @@
 
 namespace attn {
 
-template <int D_>
+template <int D_, int DT_ = kDtBF16>
 struct PrefillCfg {
   static constexpr int D = D_;
+  static constexpr bool FP8 = DT_ == kDtE4M3;
+  static constexpr int EB = FP8 ? 1 : 2;         // bytes per input element
+  static constexpr int ATOM = 128 / EB;          // elements per 128-byte swizzle atom row
   static constexpr int BM = 128;                 // rows per query tile
   static constexpr int BN = 128;                 // keys per K/V tile
-  static constexpr int NCHUNK = D / 64;          // 64-element (128-byte) swizzle atoms along d
-  static constexpr int TILE_BYTES = BN * D * 2;  // one Q, K or V tile
+  static constexpr int NCHUNK = D / ATOM;        // swizzle atoms along d
+  static constexpr int TILE_BYTES = BN * D * EB;  // one Q, K or V tile as loaded
   static constexpr int CHUNK_BYTES = BN * 128;   // one swizzle-atom column of a tile
-  static constexpr int NS = (D == 128) ? 2 : 3;  // K/V ring depth
+  static constexpr int NS = (D == 128 && !FP8) ? 2 : 3;  // K/V ring depth
+  // FP8: V widened to fp16 (two 64-column atoms per tile), double-buffered.
+  static constexpr int NVC = FP8 ? 2 : 1;
+  static constexpr int VC_BYTES = FP8 ? BN * D * 2 : 16;
   // Three full warpgroups: the third (warps 8-11: TMA, MMA, two idle) gives
   // registers to the two softmax warpgroups with setmaxnreg
   // (launch: 384 x 168 = 64512 registers; after: 256 x 200 + 128 x 96 = 63488).
@@ -66,8 +72,10 @@ struct PrefillSmem {
   alignas(1024) uint8_t q[2][C::TILE_BYTES];
   alignas(1024) uint8_t k[C::NS][C::TILE_BYTES];
   alignas(1024) uint8_t v[C::NS][C::TILE_BYTES];
+  alignas(1024) uint8_t vc[C::NVC][C::VC_BYTES];  // FP8 only: V as fp16
   uint64_t q_full, q_empty;
   uint64_t k_full[C::NS], k_empty[C::NS], v_full[C::NS], v_empty[C::NS];
+  uint64_t vc_full[C::NVC], vc_empty[C::NVC];
   uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
   uint64_t teardown;
   uint32_t tmem_base;
@@ -127,6 +135,31 @@ __device__ __forceinline__ void tanh128(float* s, float in_scale) {
     float d0, d1;
     f2_unpack(f2_add(f2_pack(e0, e1), one2), d0, d1);
     f2_unpack(f2_fma(f2_pack(rcp_approx(d0), rcp_approx(d1)), m2, one2), s[2 * i], s[2 * i + 1]);
+  }
+}
+
+// FP8: one 128-key V tile, e4m3 rows of 128 bytes (128B-swizzled as TMA
+// wrote them) -> fp16 in the MN-major layout the P.V MMA reads (two 64-column
+// 128B-swizzled atoms).  64 threads, 16 of the 1024 (row, 16-byte piece)
+// pairs each; e4m3 -> fp16 is exact.
+template <class C>
+__device__ __forceinline__ void widen_v_tile(const uint8_t* raw, uint8_t* out, int ct) {
+#pragma unroll 4
+  for (int k = 0; k < 16; ++k) {
+    const int i = ct + 64 * k;
+    const int r = i >> 3, u = i & 7;  // key row, 16-byte piece (columns 16u .. 16u+15)
+    const uint4 x = *reinterpret_cast<const uint4*>(raw + r * 128 + ((u ^ (r & 7)) << 4));
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      h[2 * j] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xffffu));
+      h[2 * j + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
+    }
+    uint8_t* atom = out + (u >> 2) * C::CHUNK_BYTES + r * 128;
+    const int p0 = 2 * (u & 3);  // 16-byte unit of columns 16u .. 16u+7 within the atom
+    *reinterpret_cast<uint4*>(atom + ((p0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(atom + (((p0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
   }
 }
 
@@ -212,7 +245,7 @@ __device__ __forceinline__ void load_paged_tile(const PrefillParams& p, const Pr
     }
 #pragma unroll
     for (int c = 0; c < C::NCHUNK; ++c)
-      tma_load_3d(dst + c * C::CHUNK_BYTES + r0 * 128, map, bar, c * 64, it.hk, row);
+      tma_load_3d(dst + c * C::CHUNK_BYTES + r0 * 128, map, bar, c * C::ATOM, it.hk, row);
   }
 }
 
@@ -291,10 +324,12 @@ __device__ __forceinline__ int item_of_round(int r) {
 
 // XF: score transform before masking (ScoreXf): none, soft-cap, ALiBi or an
 // elementwise bias (the last two are mutually exclusive with the soft-cap).
-template <int D, bool BF16, bool MASK, int XF>
-__global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
+template <int D, int DT, bool MASK, int XF>
+__global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ PrefillParams p) {
-  using C = PrefillCfg<D>;
+  using C = PrefillCfg<D, DT>;
+  constexpr bool FP8 = C::FP8;
+  constexpr bool BF16 = DT == kDtBF16;  // P / V type of the P.V MMA (FP8: fp16)
   extern __shared__ uint8_t smem_raw[];
   PrefillSmem<C>& sm = *reinterpret_cast<PrefillSmem<C>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -309,7 +344,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.v_empty[s], 1);
+      mbar_init(&sm.v_empty[s], FP8 ? 64 : 1);  // FP8: released by the 64 widening threads
+    }
+    for (int c = 0; c < C::NVC; ++c) {
+      mbar_init(&sm.vc_full[c], 64);
+      mbar_init(&sm.vc_empty[c], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
@@ -352,7 +391,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         for (int t = 0; t < 2; ++t)
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_4d(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full, c * 64,
+            tma_load_4d(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full, c * C::ATOM,
                         it.rq0 + it.m0 + t * C::BM, it.h, it.bcoord);
         ++qn;
         for (int j = 0; j < it.cnt; ++j, ++g) {
@@ -365,7 +404,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           } else {
 #pragma unroll
             for (int c = 0; c < C::NCHUNK; ++c)
-              tma_load_4d(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s], c * 64,
+              tma_load_4d(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s], c * C::ATOM,
                           it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
           }
           ++k_armed;
@@ -376,7 +415,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           } else {
 #pragma unroll
             for (int c = 0; c < C::NCHUNK; ++c)
-              tma_load_4d(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s], c * 64,
+              tma_load_4d(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s], c * C::ATOM,
                           it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
           }
           ++v_armed;
@@ -395,21 +434,27 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       }
     } else if (warp == 9 && lane == 0) {
       // ===================== MMA issuer (one thread) ===========================
-      constexpr uint32_t idesc_s = idesc_f16_f32(BF16, 128, C::BN, false, false);
+      constexpr uint32_t idesc_s =
+          FP8 ? idesc_e4m3_f32(128, C::BN) : idesc_f16_f32(BF16, 128, C::BN, false, false);
       constexpr uint32_t idesc_o = idesc_f16_f32(BF16, 128, D, false, true);
       auto issue_s = [&](int t, int g) {  // S_t = Q_t K_g^T
         const uint32_t qa = smem_u32(sm.q[t]);
         const uint32_t ka = smem_u32(sm.k[g % C::NS]);
+        // 32 bytes of d per MMA (16 fp16 / bf16 or 32 e4m3 elements).
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < D * C::EB / 32; ++k) {
           const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
-          umma_ss(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024),
-                  sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+          if constexpr (FP8)
+            umma_ss_f8(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024),
+                       sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+          else
+            umma_ss(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024),
+                    sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
         }
         umma_commit(&sm.s_full[t]);
       };
       auto issue_pv = [&](int t, int g, bool acc) {  // O_t (+)= P_t V_g
-        const uint32_t va = smem_u32(sm.v[g % C::NS]);
+        const uint32_t va = FP8 ? smem_u32(sm.vc[g % C::NVC]) : smem_u32(sm.v[g % C::NS]);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {
           umma_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8,
@@ -442,7 +487,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         for (int u = 0; ok && u < it.cnt; ++u) {
           const int gu = g + u;
           const int s = gu % C::NS;
-          if (!(ok = w.wait(&sm.v_full[s], (gu / C::NS) & 1, kErrPrefillVFull))) break;
+          if (FP8) ok = w.wait(&sm.vc_full[gu % C::NVC], (gu / C::NVC) & 1, kErrPrefillVFull);
+          else ok = w.wait(&sm.v_full[s], (gu / C::NS) & 1, kErrPrefillVFull);
+          if (!ok) break;
           const bool next = u + 1 < it.cnt;
           if (next && !(ok = w.wait(&sm.k_full[(gu + 1) % C::NS], ((gu + 1) / C::NS) & 1,
                                     kErrPrefillKFull)))
@@ -464,7 +511,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
               issue_s(t, gu + 1);
             }
           }
-          umma_commit(&sm.v_empty[s]);
+          if (FP8) umma_commit(&sm.vc_empty[gu % C::NVC]);
+          else umma_commit(&sm.v_empty[s]);
           if (next) umma_commit(&sm.k_empty[(gu + 1) % C::NS]);
           if (u == it.cnt - 2) umma_commit(&sm.q_empty);  // last S MMA issued
         }
@@ -476,8 +524,32 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       umma_commit(&sm.teardown);
       if (!wait_raw(&sm.teardown, 0, globaltimer_ns() + 50000000ull) && p.err)
         atomicOr(p.err, 1u << kErrPrefillTeardown);
+    } else if (FP8 && (warp == 10 || warp == 11)) {
+      // ============== FP8: widen each V tile from e4m3 to fp16 ================
+      // (the P.V MMA runs on the fp16 tensor path: its operands must share
+      // one type, and P keeps more precision than e4m3 that way).
+      const int ct = threadIdx.x - 320;  // 0..63
+      int g = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int item = item_of_round(r);
+        if (item >= p.num_items) break;
+        PrefillItem it;
+        if (!decode_item<C::BM, C::BN, MASK>(p, item, it) || it.cnt == 0) continue;
+        for (int j = 0; j < it.cnt; ++j, ++g) {
+          const int s = g % C::NS, c = g % C::NVC;
+          ok = __all_sync(0xffffffffu, w.wait(&sm.v_full[s], (g / C::NS) & 1, kErrPrefillVFull)) &&
+               __all_sync(0xffffffffu,
+                          w.wait(&sm.vc_empty[c], ((g / C::NVC) & 1) ^ 1, kErrPrefillVEmpty));
+          if (!ok) break;
+          widen_v_tile<C>(sm.v[s], sm.vc[c], ct);
+          fence_proxy_async_smem();  // the tensor core reads what these threads wrote
+          mbar_arrive(&sm.vc_full[c]);
+          mbar_arrive(&sm.v_empty[s]);
+        }
+      }
     }
-    // warps 10, 11 and the other lanes: no role
+    // the other lanes: no role
   } else {
     setmaxnreg_inc<200>();
     // ======================= softmax warpgroups =============================
@@ -626,37 +698,56 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         const float lse = (ltot > 0.0f) ? (mfin + __log2f(ltot)) * kLn2 : -INFINITY;
         p.lse[it.b * p.lse_batch + it.h * p.lse_head + it.rq0 + qi] = lse;
       }
-      T* obase = reinterpret_cast<T*>(p.o) + it.b * p.o_batch + it.h * p.o_head +
-                 static_cast<int64_t>(it.rq0 + mt + (warp & 3) * 32) * p.o_row;
+      constexpr int OB = FP8 ? 1 : 2;  // bytes per output element
+      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) +
+                       (it.b * p.o_batch + it.h * p.o_head +
+                        static_cast<int64_t>(it.rq0 + mt + (warp & 3) * 32) * p.o_row) * OB;
       const int rows_left = it.Lq - (mt + (warp & 3) * 32);  // valid rows of this warp
       if (have_o) {
-        // 64 columns per round: each thread packs its row into the stage
-        // (16-byte pieces, XOR-swizzled by row so a warp's stores hit distinct
-        // banks), then the warp writes 4 rows x 128 contiguous bytes per
-        // instruction instead of 32 scattered 16-byte pieces.
+        // 128 bytes of each row per round (64 fp16/bf16 or 128 e4m3 columns):
+        // each thread packs its row into the stage (16-byte pieces,
+        // XOR-swizzled by row so a warp's stores hit distinct banks), then
+        // the warp writes 4 rows x 128 contiguous bytes per instruction
+        // instead of 32 scattered 16-byte pieces.
+        constexpr int RC = 128 / OB;  // columns per round
         uint4* stage = sm.ostage[warp & 7];
         const int lr = lane & 31;
+        if constexpr (FP8) oscale *= p.o_scale;  // FP8 static quantisation: scale_p * scale_o
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 64) {
+        for (int c0 = 0; c0 < D; c0 += RC) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < RC / 32; ++h) {
             uint32_t ov[32];
             tmem_ld32(tO + c0 + 32 * h, ov);
             tmem_ld_wait();
             reg_fence(ov);
+            if constexpr (FP8) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint32_t w4[4];
+              for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t w4[4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float a = __uint_as_float(ov[8 * q4 + 2 * i]) * oscale;
-                const float bb = __uint_as_float(ov[8 * q4 + 2 * i + 1]) * oscale;
-                w4[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
+                for (int i = 0; i < 4; ++i) {
+                  const uint32_t* x = &ov[16 * q2 + 4 * i];
+                  w4[i] = pack_e4m3x4(__uint_as_float(x[0]) * oscale, __uint_as_float(x[1]) * oscale,
+                                      __uint_as_float(x[2]) * oscale, __uint_as_float(x[3]) * oscale);
+                }
+                stage[lr * 8 + ((2 * h + q2) ^ (lr & 7))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
               }
-              stage[lr * 8 + ((4 * h + q4) ^ (lr & 7))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            } else {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float a = __uint_as_float(ov[8 * q4 + 2 * i]) * oscale;
+                  const float bb = __uint_as_float(ov[8 * q4 + 2 * i + 1]) * oscale;
+                  w4[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
+                }
+                stage[lr * 8 + ((4 * h + q4) ^ (lr & 7))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
             }
           }
-          if (c0 + 64 == D) {
+          if (c0 + RC == D) {
             // O_t has been read: the next item's first P.V may overwrite it.
             tc_fence_before();
             mbar_arrive(&sm.o_free[t]);
@@ -667,15 +758,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
             const int rr = 4 * k + (lr >> 3), q = lr & 7;
             const uint4 v4 = stage[rr * 8 + (q ^ (rr & 7))];
             if (rr < rows_left)
-              *reinterpret_cast<uint4*>(obase + static_cast<int64_t>(rr) * p.o_row + c0 + 8 * q) =
-                  v4;
+              *reinterpret_cast<uint4*>(obase + (static_cast<int64_t>(rr) * p.o_row + c0) * OB +
+                                        16 * q) = v4;
           }
           __syncwarp();
         }
       } else if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(obase + static_cast<int64_t>(r & 31) * p.o_row);
+        uint4* dst = reinterpret_cast<uint4*>(obase + static_cast<int64_t>(r & 31) * p.o_row * OB);
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < D * OB / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
       }
     }
   }
@@ -688,10 +779,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool BF16, bool MASK, int XF>
+template <int D, int DT, bool MASK, int XF>
 static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream_t stream) {
-  using C = PrefillCfg<D>;
-  auto kern = attn_prefill_kernel<D, BF16, MASK, XF>;
+  using C = PrefillCfg<D, DT>;
+  auto kern = attn_prefill_kernel<D, DT, MASK, XF>;
   const int smem = static_cast<int>(sizeof(PrefillSmem<C>)) + 1024;
   static bool configured = false;  // per instantiation; attribute set is idempotent
   if (!configured) {
@@ -703,25 +794,32 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream
   return cudaGetLastError();
 }
 
-template <bool BF16, bool MASK>
+template <int DT, bool MASK>
 static cudaError_t launch_prefill_x(const PrefillParams& p, int grid, int xf,
                                    cudaStream_t stream) {
   switch (xf) {
-    case kXfNone: return launch_prefill_t<ATTN_PREFILL_D, BF16, MASK, kXfNone>(p, grid, stream);
-    case kXfSoftcap: return launch_prefill_t<ATTN_PREFILL_D, BF16, MASK, kXfSoftcap>(p, grid, stream);
-    case kXfAlibi: return launch_prefill_t<ATTN_PREFILL_D, BF16, MASK, kXfAlibi>(p, grid, stream);
-    case kXfBias: return launch_prefill_t<ATTN_PREFILL_D, BF16, MASK, kXfBias>(p, grid, stream);
+    case kXfNone: return launch_prefill_t<ATTN_PREFILL_D, DT, MASK, kXfNone>(p, grid, stream);
+    case kXfSoftcap: return launch_prefill_t<ATTN_PREFILL_D, DT, MASK, kXfSoftcap>(p, grid, stream);
+    case kXfAlibi: return launch_prefill_t<ATTN_PREFILL_D, DT, MASK, kXfAlibi>(p, grid, stream);
+    case kXfBias: return launch_prefill_t<ATTN_PREFILL_D, DT, MASK, kXfBias>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <>
-cudaError_t launch_prefill_d<ATTN_PREFILL_D>(const PrefillParams& p, int grid, bool bf16,
+cudaError_t launch_prefill_d<ATTN_PREFILL_D>(const PrefillParams& p, int grid, int dt,
                                              bool masked, int xf, cudaStream_t stream) {
-  if (bf16) return masked ? launch_prefill_x<true, true>(p, grid, xf, stream)
-                          : launch_prefill_x<true, false>(p, grid, xf, stream);
-  return masked ? launch_prefill_x<false, true>(p, grid, xf, stream)
-                : launch_prefill_x<false, false>(p, grid, xf, stream);
+  if (dt == kDtBF16) return masked ? launch_prefill_x<kDtBF16, true>(p, grid, xf, stream)
+                                   : launch_prefill_x<kDtBF16, false>(p, grid, xf, stream);
+  if (dt == kDtF16) return masked ? launch_prefill_x<kDtF16, true>(p, grid, xf, stream)
+                                  : launch_prefill_x<kDtF16, false>(p, grid, xf, stream);
+#if ATTN_PREFILL_D == 128
+  // FP8 static quantisation: head dimension 128, no score transform.
+  if (dt == kDtE4M3 && xf == kXfNone)
+    return masked ? launch_prefill_t<128, kDtE4M3, true, kXfNone>(p, grid, stream)
+                  : launch_prefill_t<128, kDtE4M3, false, kXfNone>(p, grid, stream);
+#endif
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace attn

@@ -26,7 +26,7 @@ import torch
 
 _CHUNK = 1 << 26
 
-DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
 
 
 def _randn(shape, gen, device, dtype, value_scale=1.0):

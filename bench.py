@@ -350,7 +350,34 @@ def run_extra(args, rank, pk, stream, flush, only=None):
         out.update(_extra_masks(A, inputs, pk, stream, flush, steps, warm))
     if only in (None, "chunked"):
         out.update(_extra_chunked(A, inputs, pk, stream, flush, steps, warm))
+    if only in (None, "fp8"):
+        out.update(_extra_fp8(A, inputs, pk, stream, flush, steps, warm))
     return out
+
+
+def _extra_fp8(A, inputs, pk, stream, flush, steps, warm):
+    """FP8 static quantisation on the headline shape (e4m3 Q/K/V/O, causal).
+    Roofline peak: S = Q K^T runs on the e4m3 tensor path (2x the bf16 rate,
+    nominal ratio) and P.V on the fp16 path, half of the FLOPs each, so the
+    peak is the measured bf16 peak x 4/3."""
+    import torch
+    B, H, L, d = 4, 16, 2048, 128
+    inp = inputs.dense(B, H, H, L, L, d, "e4m3", seed=1002, device="cuda", causal=True)
+    o = torch.empty_like(inp.q)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    fl = dense_flops(B, H, L, L, d, True)
+    t = time_steps(lambda: A.attn_fwd(inp.q, inp.k, inp.v, o=o, lse=lse, causal=True,
+                                      scale_p=448.0, scale_o=1.0 / 448.0), steps, warm, stream,
+                   flush)
+    ms = statistics.mean(t)
+    tf = fl / (ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops"] * 4.0 / 3.0
+    return {"fp8_e4m3_causal_prefill_B4_H16_L2048_d128": {
+        "value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+        "kernel": A.attn_last_kernel_name(),
+        "roofline": {"bound": "tensor", "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(tf / peak, 4),
+                     "peak_note": "measured bf16 x 4/3: S on e4m3 (nominal 2x), P.V on fp16"}}}
 
 
 def _extra_chunked(A, inputs, pk, stream, flush, steps, warm):
@@ -551,7 +578,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["gqa", "decode", "varlen", "masks", "chunked"],
+    ap.add_argument("--only", choices=["gqa", "decode", "varlen", "masks", "chunked", "fp8"],
                     default=None,
                     help="run one secondary workload alone (profiling) and print its line")
     ap.add_argument("--decode-batch", type=int, default=64)

@@ -57,7 +57,10 @@ typedef enum {
   ATTN_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait */
 } attn_status;
 
-typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype;
+/* ATTN_E4M3: OCP FP8 e4m3 ("fn": no infinities, max 448) for Q, K, V and O,
+ * attn_fwd and attn_fwd_varlen with d = 128 only (FP8 static quantisation,
+ * see scale_p / scale_o). */
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1, ATTN_E4M3 = 2 } attn_dtype;
 
 /* Element strides of a 4-D [batch][head][row][d] (or packed [row][head][d])
  * tensor.  d-stride is 1. */
@@ -99,6 +102,14 @@ typedef struct {
    * the scaled score (natural-log units).  NULL: off. */
   const void* bias;
   attn_strides bias_strides;
+  /* FP8 static quantisation (CK FmhaFwdFp8StaticQuantKargs), ATTN_E4M3 only:
+   * O = saturate_e4m3(scale_o * scale_p * softmax(S) V), each <= 0 meaning 1.
+   * The caller folds the Q and K dequantisation factors into scale and V's
+   * into scale_o.  P is kept in fp16 on chip (its storage type is not fixed
+   * by the pages), so scale_p changes no rounding.  No soft-cap, ALiBi or
+   * bias with ATTN_E4M3. */
+  float scale_p;
+  float scale_o;
 } attn_opts;
 /* Combinations not built: soft-cap with ALiBi or bias (the pages do not fix
  * the order), ALiBi with bias, bias outside attn_fwd: ATTN_ERR_UNSUPPORTED. */

@@ -58,9 +58,9 @@ def _lib(mutant: int = 0) -> ctypes.CDLL:
             m = [ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double]
             x = [ctypes.c_int, _D]  # top_left, alibi slopes [B][Hq]
             lib.oracle_attn_dense.argtypes = [_D, _D, _D, _D, _D] + [ctypes.c_int] * 6 + m + [
-                _D, _D, _D] + x + [_D]
+                _D, _D, _D] + x + [_D, ctypes.c_double]
             lib.oracle_attn_varlen.argtypes = [_D, _D, _D, _D, _D, _I, _I] + [ctypes.c_int] * 4 + m + [
-                _D] + x
+                _D] + x + [ctypes.c_double]
             lib.oracle_attn_paged.argtypes = [_D, _D, _D, _I, _I, _D, _D] + [ctypes.c_int] * 7 + m + [
                 _D] + x
             lib.oracle_attn_paged_partials.argtypes = [_D, _D, _D, _I, _I, _D, _D] + [
@@ -101,7 +101,7 @@ def _check(rc: int, fn: str):
 
 
 def attn_dense(q, k, v, scale, causal=False, softcap=0.0, sink=None, want_sp=False, mutant=0,
-               window=(-1, -1), top_left=False, alibi=None, bias=None):
+               window=(-1, -1), top_left=False, alibi=None, bias=None, o_scale=1.0):
     """Dense attention.  q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] -> (o [B,Hq,Lq,d], lse [B,Hq,Lq])
     and, if ``want_sp``, the materialised S and P [B,Hq,Lq,Lk].  ``alibi``: slopes
     [B,Hq] or [Hq]; ``bias``: additive bias broadcastable to [B,Hq,Lq,Lk]."""
@@ -119,7 +119,8 @@ def attn_dense(q, k, v, scale, causal=False, softcap=0.0, sink=None, want_sp=Fal
     rc = _lib(mutant).oracle_attn_dense(_p(q), _p(k), _p(v), _p(o), _p(lse), B, Hq, Hkv, Lq, Lk,
                                         d, float(scale), int(bool(causal)), int(window[0]),
                                         int(window[1]), float(softcap), _p(sk), _p(s_out),
-                                        _p(p_out), int(bool(top_left)), _p(al), _p(bi))
+                                        _p(p_out), int(bool(top_left)), _p(al), _p(bi),
+                                        float(o_scale))
     _check(rc, "attn_dense")
     if want_sp:
         return o, lse, s_out, p_out
@@ -127,7 +128,7 @@ def attn_dense(q, k, v, scale, causal=False, softcap=0.0, sink=None, want_sp=Fal
 
 
 def attn_varlen(q, k, v, cu_q, cu_k, scale, causal=False, softcap=0.0, sink=None, mutant=0,
-                window=(-1, -1), top_left=False, alibi=None):
+                window=(-1, -1), top_left=False, alibi=None, o_scale=1.0):
     """Varlen attention.  q [total_q,Hq,d], k/v [total_k,Hkv,d], cu int32 [B+1]
     -> (o [total_q,Hq,d], lse [Hq,total_q])."""
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -141,7 +142,8 @@ def attn_varlen(q, k, v, cu_q, cu_k, scale, causal=False, softcap=0.0, sink=None
     rc = _lib(mutant).oracle_attn_varlen(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(cu_q), _p(cu_k),
                                          B, Hq, Hkv, d, float(scale), int(bool(causal)),
                                          int(window[0]), int(window[1]), float(softcap), _p(sk),
-                                         int(bool(top_left)), _p(_alibi(alibi, B, Hq)))
+                                         int(bool(top_left)), _p(_alibi(alibi, B, Hq)),
+                                         float(o_scale))
     _check(rc, "attn_varlen")
     return o, lse
 

@@ -44,6 +44,12 @@
  *     batch strides): the elementwise bias is added to the scaled score.  With
  *     the soft-cap the order is not on the pages; those combinations are not
  *     evaluated (the library rejects them).
+ *   Composable Kernel, FmhaFwdFp8StaticQuantKargs and the pipeline's element
+ *     functions (P scaled by scale_p, the O accumulator scaled by scale_o and
+ *     saturated to fp8): for fp8 inputs the oracle takes the e4m3 values
+ *     exactly and returns O * o_scale with o_scale = scale_p * scale_o; the
+ *     caller rounds to e4m3.  P itself is not quantized here: its on-chip
+ *     storage type is not fixed by the page (reading stated with the kernel).
  *   FlashAttention-3 hopper/epilogue_fwd.hpp, CollectiveEpilogueFwd::store_zero:
  *     a row with no key to attend to gets O = 0 and LSE = -inf (with a sink:
  *     O = 0 and LSE = sigma).
@@ -184,7 +190,7 @@ int oracle_attn_dense(const double* q, const double* k, const double* v,
                       int B, int Hq, int Hkv, int Lq, int Lk, int d,
                       double scale, int causal, int wl, int wr, double softcap,
                       const double* sink, double* s_out, double* p_out,
-                      int top_left, const double* alibi, const double* bias)
+                      int top_left, const double* alibi, const double* bias, double o_scale)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Lq < 0 || Lk < 0 || d <= 0) return 1;
     long nbh = (long)B * Hq;
@@ -209,6 +215,8 @@ int oracle_attn_dense(const double* q, const double* k, const double* v,
                         sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
                         o + (((long)b * Hq + h) * Lq + i) * d,
                         lse + ((long)b * Hq + h) * Lq + i);
+            if (o_scale != 1.0)
+                for (int t = 0; t < d; ++t) o[(((long)b * Hq + h) * Lq + i) * d + t] *= o_scale;
             if (s_out) memcpy(s_out + (((long)b * Hq + h) * Lq + i) * Lk, s_row, sizeof(double) * Lk);
             if (p_out) memcpy(p_out + (((long)b * Hq + h) * Lq + i) * Lk, p_row, sizeof(double) * Lk);
         }
@@ -223,7 +231,7 @@ int oracle_attn_varlen(const double* q, const double* k, const double* v,
                        const int32_t* cu_q, const int32_t* cu_k,
                        int B, int Hq, int Hkv, int d,
                        double scale, int causal, int wl, int wr, double softcap,
-                       const double* sink, int top_left, const double* alibi)
+                       const double* sink, int top_left, const double* alibi, double o_scale)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0) return 1;
     int total_q = cu_q[B];
@@ -247,6 +255,8 @@ int oracle_attn_varlen(const double* q, const double* k, const double* v,
                         alibi ? alibi[(long)b * Hq + h] : 0.0,
                         sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
                         o + (row * Hq + h) * d, lse + (long)h * total_q + row);
+            if (o_scale != 1.0)
+                for (int t = 0; t < d; ++t) o[(row * Hq + h) * d + t] *= o_scale;
         }
         free(s_row); free(p_row); free(keep);
     }

@@ -65,6 +65,58 @@ def check(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     return float(err.max(initial=0.0))
 
 
+# ---------------------------------------------------------------------------
+# OCP FP8 e4m3 ("fn" variant): sign, 4 exponent bits (bias 7), 3 mantissa bits,
+# no infinities; largest finite 448 = 1.75 * 2^8; normals from 2^-6;
+# subnormals are multiples of 2^-9.  Written from that definition.
+E4M3_MAX = 448.0
+
+
+def ulp_e4m3(x: np.ndarray) -> np.ndarray:
+    """Spacing of e4m3 values at |x| (2^-9 in the subnormal range)."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -6)))
+    return np.exp2(np.maximum(e, -6.0) - 3.0)
+
+
+def round_e4m3(x: np.ndarray) -> np.ndarray:
+    """fp64 -> nearest e4m3 value (ties to even mantissa), saturated to +-448
+    (the conversion the kernel's epilogue performs, taken here in fp64)."""
+    x = np.asarray(x, dtype=np.float64)
+    q = ulp_e4m3(x)
+    r = np.round(np.abs(x) / q) * q  # numpy rounds half to even
+    return np.sign(x) * np.minimum(r, E4M3_MAX)
+
+
+def check_e4m3(o_gpu, lse_gpu, o_ref, lse_ref, what="", min_exact=0.95, o_scale=1.0, vmax=None):
+    """e4m3 output.  Before its final rounding the kernel's O differs from the
+    exact one by at most o_scale * 2^-11 * max|V| (P is rounded to fp16, a
+    relative 2^-11, before P.V; the fp32 sums add far less); the allowance
+    doubles that.  So each element must lie within one e4m3 step (at the
+    larger of the two magnitudes) plus that absolute term of the oracle
+    rounded to e4m3, and at least min_exact of them must be equal (only
+    values near a rounding boundary may differ).  LSE as for the 16-bit types."""
+    o = f64(o_gpu)
+    ref = round_e4m3(o_ref)
+    assert np.all(np.isfinite(o)), f"{what}: non-finite O"
+    err = np.abs(o - ref)
+    step = ulp_e4m3(np.maximum(np.abs(ref), np.abs(o)))
+    floor = 0.0 if vmax is None else o_scale * 2.0 ** -10 * vmax
+    bad = err > step * 1.0000001 + floor
+    assert not bad.any(), (f"{what}: O off by more than one e4m3 step + {floor} "
+                           f"(max {err.max()}, {int(bad.sum())} elements)")
+    exact = float(np.mean(err == 0.0)) if err.size else 1.0
+    assert exact >= min_exact, f"{what}: only {exact:.3f} of O equal the rounded oracle"
+    if lse_gpu is not None:
+        lg = f64(lse_gpu)
+        inf_ref = np.isneginf(lse_ref)
+        assert np.array_equal(np.isneginf(lg), inf_ref), f"{what}: -inf LSE pattern differs"
+        fin = ~inf_ref
+        if fin.any():
+            assert np.abs(lg[fin] - lse_ref[fin]).max() <= LSE_TOL, f"{what}: LSE"
+    return exact
+
+
 def no_device_error():
     bits = A.attn_device_error()
     assert bits == 0, f"device error word {bits:#x}"
