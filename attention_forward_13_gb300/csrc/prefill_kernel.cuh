@@ -57,9 +57,12 @@ struct PrefillCfg {
   // FP8: V widened to fp16 (two 64-column atoms per tile), double-buffered.
   static constexpr int NVC = FP8 ? 2 : 1;
   static constexpr int VC_BYTES = FP8 ? BN * D * 2 : 16;
-  // Three full warpgroups: the third (warps 8-11: TMA, MMA, two idle) gives
-  // registers to the two softmax warpgroups with setmaxnreg
-  // (launch: 384 x 168 = 64512 registers; after: 256 x 200 + 128 x 96 = 63488).
+  // Three full warpgroups: the third (warps 8-11: TMA, MMA, two idle or, for
+  // FP8, widening V) gives registers to the two softmax warpgroups with
+  // setmaxnreg (launch: 384 x 168 = 64512 registers; after: 256 x 192 +
+  // 128 x 120 = 64512).  The MMA thread's issue rate limits the step time, so
+  // it keeps enough registers not to spill (measured: 192/120 beats 200/96,
+  // 184/136 and 176/152 on the dense causal workloads).
   static constexpr int THREADS = 384;
   static constexpr uint32_t TM_COLS = 512;
   // Tensor-memory columns: S/P of tile t at 128*t, O of tile t at 256 + D*t.
@@ -67,15 +70,23 @@ struct PrefillCfg {
   __device__ static constexpr uint32_t tm_o(int t) { return 256u + D * t; }
 };
 
+// FP8 only: V widened to fp16 and its barriers.  An empty base for the
+// 16-bit kernels, so their shared-memory layout carries nothing for it.
+template <class C, bool FP8 = C::FP8>
+struct PrefillSmemFp8 {};
 template <class C>
-struct PrefillSmem {
+struct PrefillSmemFp8<C, true> {
+  alignas(1024) uint8_t vc[C::NVC][C::VC_BYTES];
+  uint64_t vc_full[C::NVC], vc_empty[C::NVC];
+};
+
+template <class C>
+struct PrefillSmem : PrefillSmemFp8<C> {
   alignas(1024) uint8_t q[2][C::TILE_BYTES];
   alignas(1024) uint8_t k[C::NS][C::TILE_BYTES];
   alignas(1024) uint8_t v[C::NS][C::TILE_BYTES];
-  alignas(1024) uint8_t vc[C::NVC][C::VC_BYTES];  // FP8 only: V as fp16
   uint64_t q_full, q_empty;
   uint64_t k_full[C::NS], k_empty[C::NS], v_full[C::NS], v_empty[C::NS];
-  uint64_t vc_full[C::NVC], vc_empty[C::NVC];
   uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
   uint64_t teardown;
   uint32_t tmem_base;
@@ -346,9 +357,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], FP8 ? 64 : 1);  // FP8: released by the 64 widening threads
     }
-    for (int c = 0; c < C::NVC; ++c) {
-      mbar_init(&sm.vc_full[c], 64);
-      mbar_init(&sm.vc_empty[c], 1);
+    if constexpr (FP8) {
+      for (int c = 0; c < C::NVC; ++c) {
+        mbar_init(&sm.vc_full[c], 64);
+        mbar_init(&sm.vc_empty[c], 1);
+      }
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
@@ -371,7 +384,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
   const Waiter w{globaltimer_ns() + p.timeout_ns, &sm.abort_flag, p.err};
 
   if (warp >= 8) {
-    setmaxnreg_dec<96>();
+    setmaxnreg_dec<120>();
     if (warp == 8 && lane == 0) {
       // ===================== TMA producer =====================================
       tma_prefetch_desc(&p.tm_q);
@@ -454,7 +467,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         umma_commit(&sm.s_full[t]);
       };
       auto issue_pv = [&](int t, int g, bool acc) {  // O_t (+)= P_t V_g
-        const uint32_t va = FP8 ? smem_u32(sm.vc[g % C::NVC]) : smem_u32(sm.v[g % C::NS]);
+        uint32_t va;
+        if constexpr (FP8) va = smem_u32(sm.vc[g % C::NVC]);
+        else va = smem_u32(sm.v[g % C::NS]);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {
           umma_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8,
@@ -487,7 +502,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         for (int u = 0; ok && u < it.cnt; ++u) {
           const int gu = g + u;
           const int s = gu % C::NS;
-          if (FP8) ok = w.wait(&sm.vc_full[gu % C::NVC], (gu / C::NVC) & 1, kErrPrefillVFull);
+          if constexpr (FP8) ok = w.wait(&sm.vc_full[gu % C::NVC], (gu / C::NVC) & 1, kErrPrefillVFull);
           else ok = w.wait(&sm.v_full[s], (gu / C::NS) & 1, kErrPrefillVFull);
           if (!ok) break;
           const bool next = u + 1 < it.cnt;
@@ -511,7 +526,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
               issue_s(t, gu + 1);
             }
           }
-          if (FP8) umma_commit(&sm.vc_empty[gu % C::NVC]);
+          if constexpr (FP8) umma_commit(&sm.vc_empty[gu % C::NVC]);
           else umma_commit(&sm.v_empty[s]);
           if (next) umma_commit(&sm.k_empty[(gu + 1) % C::NS]);
           if (u == it.cnt - 2) umma_commit(&sm.q_empty);  // last S MMA issued
@@ -524,7 +539,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       umma_commit(&sm.teardown);
       if (!wait_raw(&sm.teardown, 0, globaltimer_ns() + 50000000ull) && p.err)
         atomicOr(p.err, 1u << kErrPrefillTeardown);
-    } else if (FP8 && (warp == 10 || warp == 11)) {
+    } else if (warp == 10 || warp == 11) {
+      if constexpr (FP8) {
       // ============== FP8: widen each V tile from e4m3 to fp16 ================
       // (the P.V MMA runs on the fp16 tensor path: its operands must share
       // one type, and P keeps more precision than e4m3 that way).
@@ -548,10 +564,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           mbar_arrive(&sm.v_empty[s]);
         }
       }
+      }
     }
     // the other lanes: no role
   } else {
-    setmaxnreg_inc<200>();
+    setmaxnreg_inc<192>();
     // ======================= softmax warpgroups =============================
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     const int t = warp >> 2;          // query tile of this warpgroup

@@ -57,6 +57,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps (up to the hint, in ns) instead of spinning, leaving issue slots of
+// its sub-partition to the warps that work.  ATTN_WAIT_HINT_NS = 0 keeps the
+// plain try_wait.
+#ifndef ATTN_WAIT_HINT_NS
+#define ATTN_WAIT_HINT_NS 0
+#endif
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+#if ATTN_WAIT_HINT_NS > 0
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(static_cast<uint32_t>(ATTN_WAIT_HINT_NS))
+      : "memory");
+  return ok != 0;
+#else
+  return mbar_try_wait(bar, parity);
+#endif
+}
+
 // Bounded waiting.  Each CTA carries a deadline (its own start time plus the
 // launch's timeout) and a shared abort flag.  A wait that passes the deadline
 // sets the abort flag and the device error word and returns false; every other
@@ -71,7 +93,7 @@ struct Waiter {
     if (mbar_try_wait(bar, parity)) return true;
     uint32_t n = 0;
     while (true) {
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait_sleep(bar, parity)) return true;
       if ((++n & 63u) == 0) {
         if (*abort_flag) return false;
         if (globaltimer_ns() > deadline) {
