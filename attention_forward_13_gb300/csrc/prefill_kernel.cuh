@@ -445,8 +445,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         for (int jj = max(0, v_armed - C::NS); jj < v_armed; ++jj)
           wait_raw(&sm.v_full[jj % C::NS], (jj / C::NS) & 1, dl);
       }
-    } else if (warp == 9 && lane == 0) {
-      // ===================== MMA issuer (one thread) ===========================
+    } else if (warp == 9) {
+      // ===================== MMA issuer (whole warp) ==========================
+      // Every lane runs the loop; one elected lane issues each MMA and commit.
+      // Waits are voted so the warp always takes the same branch.
       constexpr uint32_t idesc_s =
           FP8 ? idesc_e4m3_f32(128, C::BN) : idesc_f16_f32(BF16, 128, C::BN, false, false);
       constexpr uint32_t idesc_o = idesc_f16_f32(BF16, 128, D, false, true);
@@ -458,13 +460,13 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         for (int k = 0; k < D * C::EB / 32; ++k) {
           const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
           if constexpr (FP8)
-            umma_ss_f8(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024),
-                       sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+            umma_ss_f8_warp(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024),
+                            sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
           else
-            umma_ss(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024),
-                    sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+            umma_ss_warp(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024),
+                         sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
         }
-        umma_commit(&sm.s_full[t]);
+        umma_commit_warp(&sm.s_full[t]);
       };
       auto issue_pv = [&](int t, int g, bool acc) {  // O_t (+)= P_t V_g
         uint32_t va;
@@ -472,9 +474,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         else va = smem_u32(sm.v[g % C::NS]);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {
-          umma_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8,
-                  sdesc_sw128(va + k * 16 * 128, C::CHUNK_BYTES, 1024), idesc_o,
-                  (acc || k > 0) ? 1u : 0u);
+          umma_ts_warp(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8,
+                       sdesc_sw128(va + k * 16 * 128, C::CHUNK_BYTES, 1024), idesc_o,
+                       (acc || k > 0) ? 1u : 0u);
         }
       };
       int g = 0, qn = 0;
@@ -486,57 +488,67 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         if (item >= p.num_items) break;
         PrefillItem it;
         if (!decode_item<C::BM, C::BN, MASK>(p, item, it) || it.cnt == 0) continue;
-        ok = w.wait(&sm.q_full, qn & 1, kErrPrefillQ) &&
-             w.wait(&sm.k_full[g % C::NS], (g / C::NS) & 1, kErrPrefillKFull);
+        ok = __all_sync(0xffffffffu, w.wait(&sm.q_full, qn & 1, kErrPrefillQ)) &&
+             __all_sync(0xffffffffu,
+                        w.wait(&sm.k_full[g % C::NS], (g / C::NS) & 1, kErrPrefillKFull));
         ++qn;
         if (!ok) break;
         tc_fence_after();
+#pragma unroll
         for (int t = 0; t < 2; ++t)
           if (it.ub[t] == 0 && it.ue[t] > 0) issue_s(t, g);
-        umma_commit(&sm.k_empty[g % C::NS]);
+        umma_commit_warp(&sm.k_empty[g % C::NS]);
         // Q is free for the next item once the item's last S MMA completes:
         // commit right after that issue so the next Q load overlaps the tail.
-        if (it.cnt == 1) umma_commit(&sm.q_empty);
+        if (it.cnt == 1) umma_commit_warp(&sm.q_empty);
         // Every streamed K/V tile is waited for and released at its step, used
         // or not (a narrow window can leave a tile to neither query tile).
         for (int u = 0; ok && u < it.cnt; ++u) {
           const int gu = g + u;
           const int s = gu % C::NS;
-          if constexpr (FP8) ok = w.wait(&sm.vc_full[gu % C::NVC], (gu / C::NVC) & 1, kErrPrefillVFull);
-          else ok = w.wait(&sm.v_full[s], (gu / C::NS) & 1, kErrPrefillVFull);
+          if constexpr (FP8)
+            ok = w.wait(&sm.vc_full[gu % C::NVC], (gu / C::NVC) & 1, kErrPrefillVFull);
+          else
+            ok = w.wait(&sm.v_full[s], (gu / C::NS) & 1, kErrPrefillVFull);
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           const bool next = u + 1 < it.cnt;
-          if (next && !(ok = w.wait(&sm.k_full[(gu + 1) % C::NS], ((gu + 1) / C::NS) & 1,
-                                    kErrPrefillKFull)))
+          if (next && !(ok = __all_sync(0xffffffffu,
+                                        w.wait(&sm.k_full[(gu + 1) % C::NS],
+                                               ((gu + 1) / C::NS) & 1, kErrPrefillKFull))))
             break;
+#pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (it.ub[t] <= u && u < it.ue[t]) {
-              if (!(ok = w.wait(&sm.p_full[t], pc[t] & 1, kErrPrefillPFull))) break;
+              if (!(ok = __all_sync(0xffffffffu, w.wait(&sm.p_full[t], pc[t] & 1, kErrPrefillPFull))))
+                break;
               ++pc[t];
               // O_t is free once the previous item's epilogue has read it.
               if (u == it.ub[t] && oc[t] > 0 &&
-                  !(ok = w.wait(&sm.o_free[t], (oc[t] - 1) & 1, kErrPrefillOFinal)))
+                  !(ok = __all_sync(0xffffffffu,
+                                    w.wait(&sm.o_free[t], (oc[t] - 1) & 1, kErrPrefillOFinal))))
                 break;
               tc_fence_after();
               issue_pv(t, gu, u > it.ub[t]);
-              if (u + 1 == it.ue[t]) umma_commit(&sm.o_final[t]);
+              if (u + 1 == it.ue[t]) umma_commit_warp(&sm.o_final[t]);
             }
             if (next && it.ub[t] <= u + 1 && u + 1 < it.ue[t]) {
               tc_fence_after();
               issue_s(t, gu + 1);
             }
           }
-          if constexpr (FP8) umma_commit(&sm.vc_empty[gu % C::NVC]);
-          else umma_commit(&sm.v_empty[s]);
-          if (next) umma_commit(&sm.k_empty[(gu + 1) % C::NS]);
-          if (u == it.cnt - 2) umma_commit(&sm.q_empty);  // last S MMA issued
+          if constexpr (FP8) umma_commit_warp(&sm.vc_empty[gu % C::NVC]);
+          else umma_commit_warp(&sm.v_empty[s]);
+          if (next) umma_commit_warp(&sm.k_empty[(gu + 1) % C::NS]);
+          if (u == it.cnt - 2) umma_commit_warp(&sm.q_empty);  // last S MMA issued
         }
+#pragma unroll
         for (int t = 0; t < 2; ++t)
           if (it.ue[t] > it.ub[t]) ++oc[t];
         g += it.cnt;
       }
-      // All MMAs this thread issued must finish before tensor memory is freed.
-      umma_commit(&sm.teardown);
+      // All MMAs this warp issued must finish before tensor memory is freed.
+      umma_commit_warp(&sm.teardown);
       if (!wait_raw(&sm.teardown, 0, globaltimer_ns() + 50000000ull) && p.err)
         atomicOr(p.err, 1u << kErrPrefillTeardown);
     } else if (warp == 10 || warp == 11) {
