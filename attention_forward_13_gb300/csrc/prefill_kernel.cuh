@@ -449,34 +449,40 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       // ===================== MMA issuer (whole warp) ==========================
       // Every lane runs the loop; one elected lane issues each MMA and commit.
       // Waits are voted so the warp always takes the same branch.
+      const uint32_t lead = elect_one() ? 1u : 0u;
       constexpr uint32_t idesc_s =
           FP8 ? idesc_e4m3_f32(128, C::BN) : idesc_f16_f32(BF16, 128, C::BN, false, false);
       constexpr uint32_t idesc_o = idesc_f16_f32(BF16, 128, D, false, true);
+      // Descriptors of the operand buffers, built once; an MMA's operand
+      // start is the buffer's plus a constant (no carry leaves the 14-bit
+      // start-address field: shared memory is below 256 KB).
+      const uint64_t qdesc0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t qdesc1 = sdesc_sw128(smem_u32(sm.q[1]), 16, 1024);
+      const uint64_t kdesc0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(sm.v[0]), C::CHUNK_BYTES, 1024);
+      constexpr uint32_t kTileDesc = C::TILE_BYTES >> 4;  // ring slot stride in descriptor units
       auto issue_s = [&](int t, int g) {  // S_t = Q_t K_g^T
-        const uint32_t qa = smem_u32(sm.q[t]);
-        const uint32_t ka = smem_u32(sm.k[g % C::NS]);
+        const uint64_t qd = t ? qdesc1 : qdesc0;
+        const uint64_t kd = kdesc0 + static_cast<uint64_t>((g % C::NS) * kTileDesc);
         // 32 bytes of d per MMA (16 fp16 / bf16 or 32 e4m3 elements).
 #pragma unroll
         for (int k = 0; k < D * C::EB / 32; ++k) {
-          const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
+          const uint32_t off = ((k >> 2) * C::CHUNK_BYTES + (k & 3) * 32) >> 4;
           if constexpr (FP8)
-            umma_ss_f8_warp(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024),
-                            sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+            umma_ss_f8_warp(tmem + C::tm_s(t), qd + off, kd + off, idesc_s, k > 0 ? 1u : 0u, lead);
           else
-            umma_ss_warp(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024),
-                         sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+            umma_ss_warp(tmem + C::tm_s(t), qd + off, kd + off, idesc_s, k > 0 ? 1u : 0u, lead);
         }
-        umma_commit_warp(&sm.s_full[t]);
+        umma_commit_warp(&sm.s_full[t], lead);
       };
       auto issue_pv = [&](int t, int g, bool acc) {  // O_t (+)= P_t V_g
-        uint32_t va;
-        if constexpr (FP8) va = smem_u32(sm.vc[g % C::NVC]);
-        else va = smem_u32(sm.v[g % C::NS]);
+        uint64_t vd;
+        if constexpr (FP8) vd = sdesc_sw128(smem_u32(sm.vc[g % C::NVC]), C::CHUNK_BYTES, 1024);
+        else vd = vdesc0 + static_cast<uint64_t>((g % C::NS) * kTileDesc);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {
-          umma_ts_warp(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8,
-                       sdesc_sw128(va + k * 16 * 128, C::CHUNK_BYTES, 1024), idesc_o,
-                       (acc || k > 0) ? 1u : 0u);
+          umma_ts_warp(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8, vd + ((k * 16 * 128) >> 4),
+                       idesc_o, (acc || k > 0) ? 1u : 0u, lead);
         }
       };
       int g = 0, qn = 0;
@@ -497,10 +503,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           if (it.ub[t] == 0 && it.ue[t] > 0) issue_s(t, g);
-        umma_commit_warp(&sm.k_empty[g % C::NS]);
+        umma_commit_warp(&sm.k_empty[g % C::NS], lead);
         // Q is free for the next item once the item's last S MMA completes:
         // commit right after that issue so the next Q load overlaps the tail.
-        if (it.cnt == 1) umma_commit_warp(&sm.q_empty);
+        if (it.cnt == 1) umma_commit_warp(&sm.q_empty, lead);
         // Every streamed K/V tile is waited for and released at its step, used
         // or not (a narrow window can leave a tile to neither query tile).
         for (int u = 0; ok && u < it.cnt; ++u) {
@@ -530,17 +536,20 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
                 break;
               tc_fence_after();
               issue_pv(t, gu, u > it.ub[t]);
-              if (u + 1 == it.ue[t]) umma_commit_warp(&sm.o_final[t]);
+              if (u + 1 == it.ue[t]) umma_commit_warp(&sm.o_final[t], lead);
             }
+            // No fence of its own: S_t(u+1) is ordered after this tile's
+            // p_full wait by the fence above (or, for a tile that starts at
+            // u+1, touches no column the softmax still reads), and its K tile
+            // by the k_full wait (copy engine to tensor core).
             if (next && it.ub[t] <= u + 1 && u + 1 < it.ue[t]) {
-              tc_fence_after();
               issue_s(t, gu + 1);
             }
           }
-          if constexpr (FP8) umma_commit_warp(&sm.vc_empty[gu % C::NVC]);
-          else umma_commit_warp(&sm.v_empty[s]);
-          if (next) umma_commit_warp(&sm.k_empty[(gu + 1) % C::NS]);
-          if (u == it.cnt - 2) umma_commit_warp(&sm.q_empty);  // last S MMA issued
+          if constexpr (FP8) umma_commit_warp(&sm.vc_empty[gu % C::NVC], lead);
+          else umma_commit_warp(&sm.v_empty[s], lead);
+          if (next) umma_commit_warp(&sm.k_empty[(gu + 1) % C::NS], lead);
+          if (u == it.cnt - 2) umma_commit_warp(&sm.q_empty, lead);  // last S MMA issued
         }
 #pragma unroll
         for (int t = 0; t < 2; ++t)
@@ -548,7 +557,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         g += it.cnt;
       }
       // All MMAs this warp issued must finish before tensor memory is freed.
-      umma_commit_warp(&sm.teardown);
+      umma_commit_warp(&sm.teardown, lead);
       if (!wait_raw(&sm.teardown, 0, globaltimer_ns() + 50000000ull) && p.err)
         atomicOr(p.err, 1u << kErrPrefillTeardown);
     } else if (warp == 10 || warp == 11) {

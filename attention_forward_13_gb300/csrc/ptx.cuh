@@ -202,42 +202,44 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Warp-wide forms of the three issue operations above: every lane of the warp
-// executes them (converged), `elect.sync` picks one lane (the lowest, lane 0
-// when all are active) and only that lane issues.  Keeping the issuing loop in
+// Warp-wide forms of the issue operations above: every lane of the warp
+// executes them (converged) and only the lane whose `leader` flag is set (one
+// lane, chosen once with elect_one()) issues.  Keeping the issuing loop in
 // converged, warp-uniform code instead of a one-lane branch lets its operand
-// arithmetic stay on the uniform datapath, which roughly doubles the issue
-// rate measured on GB300.  The elected lane is the same for every call, so
-// tcgen05.commit tracks all MMAs issued through these helpers.
+// arithmetic stay on the uniform datapath; on GB300 that cut the issue cost of
+// an MMA from ~90 to ~40 cycles in the prefill kernel.  The leader is the same
+// lane for every call, so tcgen05.commit tracks all MMAs issued through these.
 __device__ __forceinline__ void umma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
+                                             uint32_t idesc, uint32_t accumulate, uint32_t leader) {
   asm volatile(
-      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      "{\n .reg .pred p, e;\n setp.ne.b32 e, %5, 0;\n setp.ne.b32 p, %4, 0;\n"
       " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
       : "memory");
 }
 __device__ __forceinline__ void umma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
+                                             uint32_t idesc, uint32_t accumulate, uint32_t leader) {
   asm volatile(
-      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      "{\n .reg .pred p, e;\n setp.ne.b32 e, %5, 0;\n setp.ne.b32 p, %4, 0;\n"
       " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
       : "memory");
 }
 __device__ __forceinline__ void umma_ss_f8_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                uint32_t idesc, uint32_t accumulate) {
+                                                uint32_t idesc, uint32_t accumulate,
+                                                uint32_t leader) {
   asm volatile(
-      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      "{\n .reg .pred p, e;\n setp.ne.b32 e, %5, 0;\n setp.ne.b32 p, %4, 0;\n"
       " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
       : "memory");
 }
-__device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
+__device__ __forceinline__ void umma_commit_warp(uint64_t* bar, uint32_t leader) {
   asm volatile(
-      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      "{\n .reg .pred e;\n setp.ne.b32 e, %1, 0;\n"
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
-          smem_u32(bar))
+          smem_u32(bar)),
+      "r"(leader)
       : "memory");
 }
 
