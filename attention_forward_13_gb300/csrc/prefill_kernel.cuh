@@ -447,8 +447,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       }
     } else if (warp == 9) {
       // ===================== MMA issuer (whole warp) ==========================
-      // Every lane runs the loop; one elected lane issues each MMA and commit.
-      // Waits are voted so the warp always takes the same branch.
+      // Every lane runs the loop (so its operand arithmetic stays warp-uniform)
+      // and waits on the barriers itself; only the elected lane issues MMAs and
+      // commits, so lanes need no vote: nothing here is warp-synchronous.
       const uint32_t lead = elect_one() ? 1u : 0u;
       constexpr uint32_t idesc_s =
           FP8 ? idesc_e4m3_f32(128, C::BN) : idesc_f16_f32(BF16, 128, C::BN, false, false);
@@ -494,9 +495,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         if (item >= p.num_items) break;
         PrefillItem it;
         if (!decode_item<C::BM, C::BN, MASK>(p, item, it) || it.cnt == 0) continue;
-        ok = __all_sync(0xffffffffu, w.wait(&sm.q_full, qn & 1, kErrPrefillQ)) &&
-             __all_sync(0xffffffffu,
-                        w.wait(&sm.k_full[g % C::NS], (g / C::NS) & 1, kErrPrefillKFull));
+        ok = w.wait(&sm.q_full, qn & 1, kErrPrefillQ) &&
+             w.wait(&sm.k_full[g % C::NS], (g / C::NS) & 1, kErrPrefillKFull);
         ++qn;
         if (!ok) break;
         tc_fence_after();
@@ -516,23 +516,19 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
             ok = w.wait(&sm.vc_full[gu % C::NVC], (gu / C::NVC) & 1, kErrPrefillVFull);
           else
             ok = w.wait(&sm.v_full[s], (gu / C::NS) & 1, kErrPrefillVFull);
-          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           const bool next = u + 1 < it.cnt;
-          if (next && !(ok = __all_sync(0xffffffffu,
-                                        w.wait(&sm.k_full[(gu + 1) % C::NS],
-                                               ((gu + 1) / C::NS) & 1, kErrPrefillKFull))))
+          if (next && !(ok = w.wait(&sm.k_full[(gu + 1) % C::NS], ((gu + 1) / C::NS) & 1,
+                                    kErrPrefillKFull)))
             break;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (it.ub[t] <= u && u < it.ue[t]) {
-              if (!(ok = __all_sync(0xffffffffu, w.wait(&sm.p_full[t], pc[t] & 1, kErrPrefillPFull))))
-                break;
+              if (!(ok = w.wait(&sm.p_full[t], pc[t] & 1, kErrPrefillPFull))) break;
               ++pc[t];
               // O_t is free once the previous item's epilogue has read it.
               if (u == it.ub[t] && oc[t] > 0 &&
-                  !(ok = __all_sync(0xffffffffu,
-                                    w.wait(&sm.o_free[t], (oc[t] - 1) & 1, kErrPrefillOFinal))))
+                  !(ok = w.wait(&sm.o_free[t], (oc[t] - 1) & 1, kErrPrefillOFinal)))
                 break;
               tc_fence_after();
               issue_pv(t, gu, u > it.ub[t]);
