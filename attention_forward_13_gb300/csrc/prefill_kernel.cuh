@@ -646,12 +646,42 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           // CK ALiBi position encoding (slope per (batch, head), aligned like
           // the mask): natural-log score - slope*|diag - j|, in raw-score
           // units (divided by the scale folded in later).
+          // The distance |diag - j| in float from one conversion per row:
+          // the column offsets are constants and every value is an integer
+          // below 2^24, so the subtraction is exact.
           const int dq = qi + diag - j0;  // this row's diagonal, as a column
+          const float fdq = static_cast<float>(dq);
+          if (dq >= C::BN - 1 || dq <= 0) {
+            // The whole tile is on one side of the diagonal: -slope*|dq - c|
+            // is +-slope*(c - dq), two packed operations per pair of scores
+            // (an exact subtraction, then the same single-rounding FMA).
+            const float k = dq > 0 ? alibi_raw : -alibi_raw;
+            const uint64_t k2 = f2_pack(k, k), nq2 = f2_pack(-fdq, -fdq);
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = fmaf(-alibi_raw, fabsf(static_cast<float>(dq - c)), s[c]);
+            for (int i = 0; i < 64; ++i) {
+              const uint64_t d2 = f2_add(f2_pack(static_cast<float>(2 * i), static_cast<float>(2 * i + 1)), nq2);
+              f2_unpack(f2_fma(k2, d2, f2_pack(s[2 * i], s[2 * i + 1])), s[2 * i], s[2 * i + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              s[c] = fmaf(-alibi_raw, fabsf(fdq - static_cast<float>(c)), s[c]);
+          }
         } else if constexpr (XF == kXfBias) {
           // CK elementwise bias (natural-log units, added to the scaled score).
-          if (qi < it.Lq) add_bias_row<BF16>(s, bias_row + j0, it.Lk - j0, p.inv_scale);
+          if (qi < it.Lq) {
+            add_bias_row<BF16>(s, bias_row + j0, it.Lk - j0, p.inv_scale);
+            // Warm L2 with this row's bias for the next K/V tile (its valid
+            // bytes only: up to three 128-byte lines), so that next step's
+            // loads wait less.
+            if (j + 1 < nt) {
+              const char* nb = reinterpret_cast<const char*>(bias_row + j0 + C::BN);
+              const int bytes = min(it.Lk - (j0 + C::BN), C::BN) * static_cast<int>(sizeof(T));
+              prefetch_l2(nb);
+              if (bytes > 128) prefetch_l2(nb + 128);
+              prefetch_l2(nb + bytes - 1);
+            }
+          }
         }
         if ((j0 + C::BN > it.Lk) ||
             (MASK && p.win_right >= 0 && j0 + C::BN - 1 > mt + diag + p.win_right) ||
@@ -659,8 +689,13 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           int hi = it.Lk - 1 - j0, lo = 0;  // kept columns [lo, hi] of this row
           if (MASK && p.win_right >= 0) hi = min(hi, qi + diag + p.win_right - j0);
           if (MASK && p.win_left >= 0) lo = qi + diag - p.win_left - j0;
+          if (lo <= 0) {  // no left bound inside the tile (plain causal or the tail)
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : -INFINITY;
+            for (int c = 0; c < 128; ++c) s[c] = c <= hi ? s[c] : -INFINITY;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : -INFINITY;
+          }
         }
         const float m_new = fmaxf(m_use, max128(s) * a_coef);  // a_coef > 0: order kept
         float alpha = 1.0f;

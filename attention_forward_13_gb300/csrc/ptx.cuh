@@ -107,6 +107,12 @@ struct Waiter {
   __device__ __forceinline__ bool aborted() const { return *abort_flag != 0; }
 };
 
+// Hint: bring the 128-byte line holding `addr` into L2 (no data returned, no
+// fault on any address the caller may read).
+__device__ __forceinline__ void prefetch_l2(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 // ----------------------------------------------------------------------------
 // TMA (tensor copies global -> shared, completion on an mbarrier)
 // ----------------------------------------------------------------------------
