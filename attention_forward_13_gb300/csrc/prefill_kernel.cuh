@@ -70,6 +70,10 @@ struct PrefillCfg {
   __device__ static constexpr uint32_t tm_o(int t) { return 256u + D * t; }
 };
 
+// Group mode / paged cache: most (query block, sequence) slots the per-CTA
+// work-order sort handles (more: the plain order).
+constexpr int kMaxSlots = 2048;
+
 // FP8 only: V widened to fp16 and its barriers.  An empty base for the
 // 16-bit kernels, so their shared-memory layout carries nothing for it.
 template <class C, bool FP8 = C::FP8>
@@ -91,9 +95,15 @@ struct PrefillSmem : PrefillSmemFp8<C> {
   uint64_t teardown;
   uint32_t tmem_base;
   int abort_flag;
-  // Epilogue staging, one 32-row x 128-byte block per softmax warp: rows go
-  // in from the thread that owns them and out as whole 128-byte lines.
-  alignas(128) uint4 ostage[8][32 * 8];
+  // Epilogue staging, one 32-row x 64-byte block per softmax warp: rows go
+  // in from the thread that owns them and out as 64-byte row pieces.
+  alignas(128) uint4 ostage[8][32 * 4];
+  // Group-mode / paged work order (order_items): slots heaviest first, each
+  // slot's cost while sorting, per-cost bucket cursors, slots in use.
+  uint16_t slot_order[kMaxSlots];
+  uint8_t slot_cost[kMaxSlots];
+  int cost_cursor[256];
+  int n_slots;
 };
 
 // Maximum of 128 values: a tree of 3-input max instructions (64 instructions,
@@ -267,13 +277,10 @@ __device__ __forceinline__ void load_paged_tile(const PrefillParams& p, const Pr
 // from the left/right window): i + (Lk - Lq) - win_left <= j <= i + (Lk - Lq)
 // + win_right, a negative bound meaning unbounded; causal is win_right = 0.
 template <int BM, int BN, bool MASK>
-__device__ __forceinline__ bool decode_item(const PrefillParams& p, int item, PrefillItem& it) {
-  const int nbh = p.B * p.Hq;
-  const int mb_i = item / nbh;
-  const int bh = item - mb_i * nbh;
-  const int mb = MASK ? (p.num_m_blocks - 1 - mb_i) : mb_i;
-  it.h = bh % p.Hq;
-  it.b = bh / p.Hq;
+__device__ __forceinline__ bool decode_pair(const PrefillParams& p, int b, int mb, int h,
+                                            PrefillItem& it) {
+  it.h = h;
+  it.b = b;
   it.hk = it.h / (p.Hq / p.Hkv);
   it.Lq = p.Lq;
   it.Lk = p.Lk;
@@ -326,6 +333,94 @@ __device__ __forceinline__ bool decode_item(const PrefillParams& p, int item, Pr
   return true;
 }
 
+// Work-item order.  Dense problems keep the plain order: query block (the
+// heaviest causal blocks first), then (batch, head).  In group mode and over a
+// paged cache the sequences differ in length, so that order leaves holes
+// (blocks past a short sequence's end) and mixes costs; there every CTA sorts
+// the (query block, sequence) slots by their K/V step count, heaviest first,
+// and items become (slot, head) in that order.
+struct ItemOrder {
+  const uint16_t* slot;  // slot = query block * B + sequence, heaviest first
+  int n;                 // slots in use; -1: plain order
+};
+
+template <int BM, int BN, bool MASK, bool ORD>
+__device__ __forceinline__ bool decode_item(const PrefillParams& p, const ItemOrder& ord, int item,
+                                            PrefillItem& it) {
+  if constexpr (ORD) {
+    if (ord.n >= 0) {
+      const int pos = item / p.Hq;
+      if (pos >= ord.n) return false;
+      const int slot = ord.slot[pos];
+      const int mb = slot / p.B;
+      return decode_pair<BM, BN, MASK>(p, slot - mb * p.B, mb, item - pos * p.Hq, it);
+    }
+  }
+  const int nbh = p.B * p.Hq;
+  const int mb_i = item / nbh;
+  const int bh = item - mb_i * nbh;
+  const int mb = MASK ? (p.num_m_blocks - 1 - mb_i) : mb_i;
+  return decode_pair<BM, BN, MASK>(p, bh / p.Hq, mb, bh % p.Hq, it);
+}
+
+// Builds the group-mode / paged work order in shared memory; every thread of
+// the CTA calls it (it synchronises the block).  Costs are K/V steps + 1
+// (a slot with rows but no key still writes its output), 0 for a slot past
+// its sequence's end; a histogram gives each cost's first position, heaviest
+// first, and one warp places the slots in slot order within a cost, so that
+// every CTA builds the same list.
+template <int BM, int BN, bool MASK, class C>
+__device__ void order_items(const PrefillParams& p, PrefillSmem<C>& sm) {
+  const int nslots = p.num_m_blocks * p.B;
+  if ((p.cu_q == nullptr && p.seqlens_k == nullptr) || nslots > kMaxSlots) {
+    if (threadIdx.x == 0) sm.n_slots = -1;
+    __syncthreads();
+    return;
+  }
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) sm.cost_cursor[i] = 0;
+  __syncthreads();
+  for (int s = threadIdx.x; s < nslots; s += blockDim.x) {
+    PrefillItem it;
+    const int mb = s / p.B;
+    int c = 0;
+    if (decode_pair<BM, BN, MASK>(p, s - mb * p.B, mb, 0, it)) c = min(it.cnt, 254) + 1;
+    sm.slot_cost[s] = static_cast<uint8_t>(c);
+    if (c > 0) atomicAdd(&sm.cost_cursor[c], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    // First position of each cost, heaviest first (costs 255 .. 1, 32 at a time).
+    int run = 0;
+    for (int c0 = 255; c0 > 0; c0 -= 32) {
+      const int c = c0 - lane;
+      const int v = c > 0 ? sm.cost_cursor[c] : 0;
+      int x = v;  // inclusive prefix over the lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (c > 0) sm.cost_cursor[c] = run + x - v;
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    __syncwarp();
+    // Place the slots 32 at a time; equal costs keep slot order.
+    for (int s0 = 0; s0 < nslots; s0 += 32) {
+      const int s = s0 + lane;
+      const int c = s < nslots ? sm.slot_cost[s] : 0;
+      const unsigned same = __match_any_sync(0xffffffffu, c);
+      const int rank = __popc(same & ((1u << lane) - 1u));
+      if (c > 0) sm.slot_order[sm.cost_cursor[c] + rank] = static_cast<uint16_t>(s);
+      __syncwarp();
+      if (c > 0 && rank == __popc(same) - 1) sm.cost_cursor[c] += __popc(same);
+      __syncwarp();
+    }
+    if (lane == 0) sm.n_slots = run;
+  }
+  __syncthreads();
+}
+
 // The r-th item of this CTA: rounds of gridDim.x items, alternating direction
 // (snake), so the heavy head of the list is spread evenly across CTAs.
 __device__ __forceinline__ int item_of_round(int r) {
@@ -335,7 +430,8 @@ __device__ __forceinline__ int item_of_round(int r) {
 
 // XF: score transform before masking (ScoreXf): none, soft-cap, ALiBi or an
 // elementwise bias (the last two are mutually exclusive with the soft-cap).
-template <int D, int DT, bool MASK, int XF>
+// ORD: group mode or paged cache, work items in the sorted order (order_items).
+template <int D, int DT, bool MASK, int XF, bool ORD>
 __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = PrefillCfg<D, DT>;
@@ -380,6 +476,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  ItemOrder ord{nullptr, -1};
+  if constexpr (ORD) {
+    order_items<C::BM, C::BN, MASK>(p, sm);
+    ord = ItemOrder{sm.slot_order, sm.n_slots};
+  }
   const uint32_t tmem = sm.tmem_base;
   const Waiter w{globaltimer_ns() + p.timeout_ns, &sm.abort_flag, p.err};
 
@@ -396,7 +497,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         const int item = item_of_round(r);
         if (item >= p.num_items) break;
         PrefillItem it;
-        if (!decode_item<C::BM, C::BN, MASK>(p, item, it) || it.cnt == 0) continue;
+        if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it) || it.cnt == 0) continue;
         // The previous item's S MMAs must be done with the Q buffer.
         if (qn > 0 && !(ok = w.wait(&sm.q_empty, (qn - 1) & 1, kErrPrefillQ))) break;
         mbar_arrive_expect_tx(&sm.q_full, 2 * C::TILE_BYTES);
@@ -494,7 +595,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         const int item = item_of_round(r);
         if (item >= p.num_items) break;
         PrefillItem it;
-        if (!decode_item<C::BM, C::BN, MASK>(p, item, it) || it.cnt == 0) continue;
+        if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it) || it.cnt == 0) continue;
         ok = w.wait(&sm.q_full, qn & 1, kErrPrefillQ) &&
              w.wait(&sm.k_full[g % C::NS], (g / C::NS) & 1, kErrPrefillKFull);
         ++qn;
@@ -568,7 +669,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         const int item = item_of_round(r);
         if (item >= p.num_items) break;
         PrefillItem it;
-        if (!decode_item<C::BM, C::BN, MASK>(p, item, it) || it.cnt == 0) continue;
+        if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it) || it.cnt == 0) continue;
         for (int j = 0; j < it.cnt; ++j, ++g) {
           const int s = g % C::NS, c = g % C::NVC;
           ok = __all_sync(0xffffffffu, w.wait(&sm.v_full[s], (g / C::NS) & 1, kErrPrefillVFull)) &&
@@ -599,7 +700,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       const int item = item_of_round(rr);
       if (item >= p.num_items) break;
       PrefillItem it;
-      if (!decode_item<C::BM, C::BN, MASK>(p, item, it)) continue;
+      if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it)) continue;
       const int mt = it.m0 + t * C::BM;
       if (mt >= it.Lq) continue;  // this tile has no row
       const int qi = mt + r;      // query index within the sequence
@@ -773,12 +874,12 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
                         static_cast<int64_t>(it.rq0 + mt + (warp & 3) * 32) * p.o_row) * OB;
       const int rows_left = it.Lq - (mt + (warp & 3) * 32);  // valid rows of this warp
       if (have_o) {
-        // 128 bytes of each row per round (64 fp16/bf16 or 128 e4m3 columns):
-        // each thread packs its row into the stage (16-byte pieces,
-        // XOR-swizzled by row so a warp's stores hit distinct banks), then
-        // the warp writes 4 rows x 128 contiguous bytes per instruction
+        // 64 bytes of each row per round (32 fp16/bf16 or 64 e4m3 columns):
+        // each thread packs its row into the stage (16-byte pieces, XOR-
+        // swizzled by row pair so 8 consecutive rows hit distinct banks),
+        // then the warp writes 8 rows x 64 contiguous bytes per instruction
         // instead of 32 scattered 16-byte pieces.
-        constexpr int RC = 128 / OB;  // columns per round
+        constexpr int RC = 64 / OB;  // columns per round
         uint4* stage = sm.ostage[warp & 7];
         const int lr = lane & 31;
         if constexpr (FP8) oscale *= p.o_scale;  // FP8 static quantisation: scale_p * scale_o
@@ -800,7 +901,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
                   w4[i] = pack_e4m3x4(__uint_as_float(x[0]) * oscale, __uint_as_float(x[1]) * oscale,
                                       __uint_as_float(x[2]) * oscale, __uint_as_float(x[3]) * oscale);
                 }
-                stage[lr * 8 + ((2 * h + q2) ^ (lr & 7))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                stage[lr * 4 + ((2 * h + q2) ^ ((lr >> 1) & 3))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
               }
             } else {
 #pragma unroll
@@ -812,7 +913,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
                   const float bb = __uint_as_float(ov[8 * q4 + 2 * i + 1]) * oscale;
                   w4[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
                 }
-                stage[lr * 8 + ((4 * h + q4) ^ (lr & 7))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                stage[lr * 4 + (q4 ^ ((lr >> 1) & 3))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
               }
             }
           }
@@ -823,9 +924,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           }
           __syncwarp();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int rr = 4 * k + (lr >> 3), q = lr & 7;
-            const uint4 v4 = stage[rr * 8 + (q ^ (rr & 7))];
+          for (int k = 0; k < 4; ++k) {
+            const int rr = 8 * k + (lr >> 2), q = lr & 3;
+            const uint4 v4 = stage[rr * 4 + (q ^ ((rr >> 1) & 3))];
             if (rr < rows_left)
               *reinterpret_cast<uint4*>(obase + (static_cast<int64_t>(rr) * p.o_row + c0) * OB +
                                         16 * q) = v4;
@@ -848,10 +949,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
   }
 }
 
-template <int D, int DT, bool MASK, int XF>
+template <int D, int DT, bool MASK, int XF, bool ORD = false>
 static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream_t stream) {
   using C = PrefillCfg<D, DT>;
-  auto kern = attn_prefill_kernel<D, DT, MASK, XF>;
+  auto kern = attn_prefill_kernel<D, DT, MASK, XF, ORD>;
   const int smem = static_cast<int>(sizeof(PrefillSmem<C>)) + 1024;
   static bool configured = false;  // per instantiation; attribute set is idempotent
   if (!configured) {
@@ -866,6 +967,16 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream
 template <int DT, bool MASK>
 static cudaError_t launch_prefill_x(const PrefillParams& p, int grid, int xf,
                                    cudaStream_t stream) {
+  // Group mode and paged caches take the sorted work order (no bias there).
+  if (p.cu_q != nullptr || p.seqlens_k != nullptr) {
+    switch (xf) {
+      case kXfNone: return launch_prefill_t<ATTN_PREFILL_D, DT, MASK, kXfNone, true>(p, grid, stream);
+      case kXfSoftcap:
+        return launch_prefill_t<ATTN_PREFILL_D, DT, MASK, kXfSoftcap, true>(p, grid, stream);
+      case kXfAlibi: return launch_prefill_t<ATTN_PREFILL_D, DT, MASK, kXfAlibi, true>(p, grid, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (xf) {
     case kXfNone: return launch_prefill_t<ATTN_PREFILL_D, DT, MASK, kXfNone>(p, grid, stream);
     case kXfSoftcap: return launch_prefill_t<ATTN_PREFILL_D, DT, MASK, kXfSoftcap>(p, grid, stream);
@@ -884,9 +995,13 @@ cudaError_t launch_prefill_d<ATTN_PREFILL_D>(const PrefillParams& p, int grid, i
                                   : launch_prefill_x<kDtF16, false>(p, grid, xf, stream);
 #if ATTN_PREFILL_D == 128
   // FP8 static quantisation: head dimension 128, no score transform.
-  if (dt == kDtE4M3 && xf == kXfNone)
+  if (dt == kDtE4M3 && xf == kXfNone) {
+    if (p.cu_q != nullptr)
+      return masked ? launch_prefill_t<128, kDtE4M3, true, kXfNone, true>(p, grid, stream)
+                    : launch_prefill_t<128, kDtE4M3, false, kXfNone, true>(p, grid, stream);
     return masked ? launch_prefill_t<128, kDtE4M3, true, kXfNone>(p, grid, stream)
                   : launch_prefill_t<128, kDtE4M3, false, kXfNone>(p, grid, stream);
+  }
 #endif
   return cudaErrorInvalidValue;
 }
