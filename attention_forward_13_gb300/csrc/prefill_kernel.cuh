@@ -14,12 +14,15 @@
 // fold).  The Blackwell design here differs from all three:
 //
 //  * persistent: one CTA per SM walks a list of work items (a 256-row query
-//    block of one (batch, head)), heaviest causal blocks first, in snake
-//    order across CTAs.  The next item's Q load and its first S = Q K^T
-//    overlap the current item's last P.V and epilogue.
+//    block of one (batch, head)) in snake order across CTAs: heaviest causal
+//    blocks first for dense problems; in group mode and over a paged cache
+//    every CTA first sorts the (query block, sequence) pairs by cost.  The
+//    next item's Q load and its first S = Q K^T overlap the current item's
+//    last P.V and epilogue.
 //  * each item is two 128-row query tiles sharing every 128-key K/V tile;
 //    warps 0-3 run the softmax of tile 0, warps 4-7 that of tile 1, warp 8
-//    issues TMA, warp 9 issues tcgen05.mma.  While one warpgroup computes
+//    issues TMA, warp 9 issues tcgen05.mma (the whole warp runs the loop, one
+//    elected lane issues).  While one warpgroup computes
 //    exponentials the tensor core works on the other tile (ping-pong).
 //  * S lives in tensor memory (fp32, 128 columns per tile).  The softmax
 //    writes P (bf16/fp16) back over the first 64 columns of its S and the
@@ -60,7 +63,7 @@ struct PrefillCfg {
   // Three full warpgroups: the third (warps 8-11: TMA, MMA, two idle or, for
   // FP8, widening V) gives registers to the two softmax warpgroups with
   // setmaxnreg (launch: 384 x 168 = 64512 registers; after: 256 x 192 +
-  // 128 x 120 = 64512).  The MMA thread's issue rate limits the step time, so
+  // 128 x 120 = 64512).  The MMA warp's issue rate limits the step time, so
   // it keeps enough registers not to spill (measured: 192/120 beats 200/96,
   // 184/136 and 176/152 on the dense causal workloads).
   static constexpr int THREADS = 384;
