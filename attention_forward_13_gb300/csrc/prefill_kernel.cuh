@@ -92,7 +92,7 @@ struct PrefillSmem : PrefillSmemFp8<C> {
   alignas(1024) uint8_t q[2][C::TILE_BYTES];
   alignas(1024) uint8_t k[C::NS][C::TILE_BYTES];
   alignas(1024) uint8_t v[C::NS][C::TILE_BYTES];
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];  // per query tile
   uint64_t k_full[C::NS], k_empty[C::NS], v_full[C::NS], v_empty[C::NS];
   uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
   uint64_t teardown;
@@ -448,8 +448,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_empty, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.q_full[t], 1);
+      mbar_init(&sm.q_empty[t], 1);
+    }
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
@@ -495,21 +497,26 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       int g = 0, qn = 0, k_armed = 0, v_armed = 0;
+      int qa[2] = {0, 0};  // arms of each tile's q_full
       bool ok = true;
       for (int r = 0; ok; ++r) {
         const int item = item_of_round(r);
         if (item >= p.num_items) break;
         PrefillItem it;
         if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it) || it.cnt == 0) continue;
-        // The previous item's S MMAs must be done with the Q buffer.
-        if (qn > 0 && !(ok = w.wait(&sm.q_empty, (qn - 1) & 1, kErrPrefillQ))) break;
-        mbar_arrive_expect_tx(&sm.q_full, 2 * C::TILE_BYTES);
+        // Each tile's Q buffer is reloaded once the previous item's last S
+        // MMA of that tile is done (tile 0 usually a step before tile 1).
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+        for (int t = 0; t < 2; ++t) {
+          if (qn > 0 && !(ok = w.wait(&sm.q_empty[t], (qn - 1) & 1, kErrPrefillQ))) break;
+          mbar_arrive_expect_tx(&sm.q_full[t], C::TILE_BYTES);
+          ++qa[t];
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_4d(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full, c * C::ATOM,
+            tma_load_4d(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full[t], c * C::ATOM,
                         it.rq0 + it.m0 + t * C::BM, it.h, it.bcoord);
+        }
+        if (!ok) break;
         ++qn;
         for (int j = 0; j < it.cnt; ++j, ++g) {
           const int s = g % C::NS;
@@ -543,7 +550,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         // is released.  The last armed phase of each full barrier completes
         // when its bytes arrive.
         const uint64_t dl = globaltimer_ns() + 50000000ull;
-        if (qn > 0) wait_raw(&sm.q_full, (qn - 1) & 1, dl);
+        for (int t = 0; t < 2; ++t)
+          if (qa[t] > 0) wait_raw(&sm.q_full[t], (qa[t] - 1) & 1, dl);
         for (int jj = max(0, k_armed - C::NS); jj < k_armed; ++jj)
           wait_raw(&sm.k_full[jj % C::NS], (jj / C::NS) & 1, dl);
         for (int jj = max(0, v_armed - C::NS); jj < v_armed; ++jj)
@@ -599,18 +607,20 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         if (item >= p.num_items) break;
         PrefillItem it;
         if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it) || it.cnt == 0) continue;
-        ok = w.wait(&sm.q_full, qn & 1, kErrPrefillQ) &&
-             w.wait(&sm.k_full[g % C::NS], (g / C::NS) & 1, kErrPrefillKFull);
+        ok = w.wait(&sm.k_full[g % C::NS], (g / C::NS) & 1, kErrPrefillKFull);
+        // Each tile's first S as soon as its Q is in; a tile's Q buffer is
+        // free for the next item once its last S MMA completes: commit right
+        // after that issue so the next Q load overlaps the tail.
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || !(ok = w.wait(&sm.q_full[t], qn & 1, kErrPrefillQ))) break;
+          tc_fence_after();
+          if (it.ub[t] == 0 && it.ue[t] > 0) issue_s(t, g);
+          if (it.ue[t] <= 1) umma_commit_warp(&sm.q_empty[t], lead);  // no later S for tile t
+        }
         ++qn;
         if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (it.ub[t] == 0 && it.ue[t] > 0) issue_s(t, g);
         umma_commit_warp(&sm.k_empty[g % C::NS], lead);
-        // Q is free for the next item once the item's last S MMA completes:
-        // commit right after that issue so the next Q load overlaps the tail.
-        if (it.cnt == 1) umma_commit_warp(&sm.q_empty, lead);
         // Every streamed K/V tile is waited for and released at its step, used
         // or not (a narrow window can leave a tile to neither query tile).
         for (int u = 0; ok && u < it.cnt; ++u) {
@@ -644,12 +654,12 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
             // by the k_full wait (copy engine to tensor core).
             if (next && it.ub[t] <= u + 1 && u + 1 < it.ue[t]) {
               issue_s(t, gu + 1);
+              if (u + 2 == it.ue[t]) umma_commit_warp(&sm.q_empty[t], lead);  // tile t's last S
             }
           }
           if constexpr (FP8) umma_commit_warp(&sm.vc_empty[gu % C::NVC], lead);
           else umma_commit_warp(&sm.v_empty[s], lead);
           if (next) umma_commit_warp(&sm.k_empty[(gu + 1) % C::NS], lead);
-          if (u == it.cnt - 2) umma_commit_warp(&sm.q_empty, lead);  // last S MMA issued
         }
 #pragma unroll
         for (int t = 0; t < 2; ++t)
