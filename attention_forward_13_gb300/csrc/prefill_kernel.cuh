@@ -887,53 +887,51 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
                         static_cast<int64_t>(it.rq0 + mt + (warp & 3) * 32) * p.o_row) * OB;
       const int rows_left = it.Lq - (mt + (warp & 3) * 32);  // valid rows of this warp
       if (have_o) {
-        // 64 bytes of each row per round (32 fp16/bf16 or 64 e4m3 columns):
-        // each thread packs its row into the stage (16-byte pieces, XOR-
-        // swizzled by row pair so 8 consecutive rows hit distinct banks),
-        // then the warp writes 8 rows x 64 contiguous bytes per instruction
-        // instead of 32 scattered 16-byte pieces.
+        // O is read from tensor memory first; then 64 bytes of each row per
+        // round (32 fp16/bf16 or 64 e4m3 columns): each thread packs its row
+        // into the stage (16-byte pieces, XOR-swizzled by row pair so 8
+        // consecutive rows hit distinct banks), then the warp writes 8 rows x
+        // 64 contiguous bytes per instruction instead of 32 scattered 16-byte
+        // pieces.
         constexpr int RC = 64 / OB;  // columns per round
         uint4* stage = sm.ostage[warp & 7];
         const int lr = lane & 31;
         if constexpr (FP8) oscale *= p.o_scale;  // FP8 static quantisation: scale_p * scale_o
+        // All of O_t at once (one wait), then O_t goes back to the MMA warp
+        // before any packing or store.
+        uint32_t ov[D];
+#pragma unroll
+        for (int c = 0; c < D; c += 32) tmem_ld32(tO + c, *reinterpret_cast<uint32_t(*)[32]>(&ov[c]));
+        tmem_ld_wait();
+        reg_fence(ov);
+        tc_fence_before();
+        mbar_arrive(&sm.o_free[t]);
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += RC) {
+          if constexpr (FP8) {
 #pragma unroll
-          for (int h = 0; h < RC / 32; ++h) {
-            uint32_t ov[32];
-            tmem_ld32(tO + c0 + 32 * h, ov);
-            tmem_ld_wait();
-            reg_fence(ov);
-            if constexpr (FP8) {
+            for (int q = 0; q < 4; ++q) {  // 16 e4m3 columns per 16-byte piece
+              uint32_t w4[4];
 #pragma unroll
-              for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const uint32_t* x = &ov[16 * q2 + 4 * i];
-                  w4[i] = pack_e4m3x4(__uint_as_float(x[0]) * oscale, __uint_as_float(x[1]) * oscale,
-                                      __uint_as_float(x[2]) * oscale, __uint_as_float(x[3]) * oscale);
-                }
-                stage[lr * 4 + ((2 * h + q2) ^ ((lr >> 1) & 3))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t* x = &ov[c0 + 16 * q + 4 * i];
+                w4[i] = pack_e4m3x4(__uint_as_float(x[0]) * oscale, __uint_as_float(x[1]) * oscale,
+                                    __uint_as_float(x[2]) * oscale, __uint_as_float(x[3]) * oscale);
               }
-            } else {
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float a = __uint_as_float(ov[8 * q4 + 2 * i]) * oscale;
-                  const float bb = __uint_as_float(ov[8 * q4 + 2 * i + 1]) * oscale;
-                  w4[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
-                }
-                stage[lr * 4 + (q4 ^ ((lr >> 1) & 3))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-              }
+              stage[lr * 4 + (q ^ ((lr >> 1) & 3))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-          }
-          if (c0 + RC == D) {
-            // O_t has been read: the next item's first P.V may overwrite it.
-            tc_fence_before();
-            mbar_arrive(&sm.o_free[t]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // 8 fp16/bf16 columns per 16-byte piece
+              uint32_t w4[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float a = __uint_as_float(ov[c0 + 8 * q + 2 * i]) * oscale;
+                const float bb = __uint_as_float(ov[c0 + 8 * q + 2 * i + 1]) * oscale;
+                w4[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
+              }
+              stage[lr * 4 + (q ^ ((lr >> 1) & 3))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
           }
           __syncwarp();
 #pragma unroll
