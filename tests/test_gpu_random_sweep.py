@@ -156,3 +156,58 @@ def test_random_paged(case):
                                alibi=None if sl is None else sl.numpy())
     check(o, lse, ro, rl, f"paged {case}")
     no_device_error()
+
+
+def _fp8_cases(n):
+    rng = np.random.default_rng(SEED + 3)
+    out = []
+    for _ in range(n):
+        varlen = bool(rng.integers(2))
+        Hkv = int(rng.choice([1, 2]))
+        g = int(rng.choice([1, 2, 4]))
+        causal = bool(rng.integers(2))
+        win = None
+        if rng.random() < 0.3:
+            win = (int(rng.integers(0, 300)), int(rng.choice([-1, 0])))
+        sp = float(rng.choice([1.0, 448.0]))
+        so = float(rng.choice([1.0, 2.0])) / sp
+        if varlen:
+            B = int(rng.integers(1, 5))
+            shape = ([int(x) for x in rng.integers(0, 400, B)],)
+        else:
+            Lq = int(rng.integers(1, 513))
+            shape = (int(rng.integers(1, 3)), Lq, Lq if rng.random() < 0.5 else int(rng.integers(1, 513)))
+        out.append((varlen, shape, Hkv * g, Hkv, causal, win, sp, so, int(rng.integers(1 << 30))))
+    return out
+
+
+FP8 = _fp8_cases(8)
+
+
+@pytest.mark.parametrize("case", FP8, ids=[f"fp8_{i}" for i in range(len(FP8))])
+def test_random_fp8(case):
+    """FP8 e4m3 static quantisation (d = 128), dense or group mode: O within
+    one e4m3 step of the rounded oracle (scale_p * scale_o applied)."""
+    from tests._parity import check_e4m3
+    varlen, shape, Hq, Hkv, causal, win, sp, so, seed = case
+    if varlen:
+        (lens,) = shape
+        inp = inputs.varlen(lens, lens, Hq, Hkv, 128, "e4m3", seed=seed, causal=causal)
+        o, lse = A.attn_fwd_varlen(cuda(inp.q), cuda(inp.k), cuda(inp.v), cuda(inp.cu_seqlens_q),
+                                   cuda(inp.cu_seqlens_k), inp.max_seqlen_q, causal=causal,
+                                   window=win, scale_p=sp, scale_o=so)
+        torch.cuda.synchronize()
+        ro, rl = oracle.attn_varlen(f64(inp.q), f64(inp.k), f64(inp.v), inp.cu_seqlens_q.numpy(),
+                                    inp.cu_seqlens_k.numpy(), 1 / math.sqrt(128), causal,
+                                    window=win if win else (-1, -1), o_scale=sp * so)
+    else:
+        B, Lq, Lk = shape
+        inp = inputs.dense(B, Hq, Hkv, Lq, Lk, 128, "e4m3", seed=seed, causal=causal)
+        o, lse = A.attn_fwd(cuda(inp.q), cuda(inp.k), cuda(inp.v), causal=causal, window=win,
+                            scale_p=sp, scale_o=so)
+        torch.cuda.synchronize()
+        ro, rl = oracle.attn_dense(f64(inp.q), f64(inp.k), f64(inp.v), 1 / math.sqrt(128), causal,
+                                   window=win if win else (-1, -1), o_scale=sp * so)
+    check_e4m3(o, lse, ro, rl, f"fp8 {case}", o_scale=sp * so,
+               vmax=float(np.abs(f64(inp.v)).max()) if f64(inp.v).size else 0.0)
+    no_device_error()
