@@ -7,11 +7,17 @@
 #include "launch.h"
 #include "ptx.cuh"
 
+#include <algorithm>
+#include <array>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <memory>
 #include <mutex>
+#include <vector>
 
 using namespace attn;
 
@@ -241,6 +247,139 @@ cudaError_t launch_selftest_timeout(unsigned int* err, unsigned long long timeou
 }
 }  // namespace attn
 
+namespace {
+
+// Static schedule for dense masked prefill.  With a causal or window mask the
+// query blocks of one (batch, head) cost different numbers of K/V steps, and
+// the snake order over the plain item list leaves some CTAs a block more than
+// others at the end.  Here the host packs the items onto the grid once per
+// shape: longest processing time first (each item to the least loaded CTA),
+// then single moves and pairwise swaps off the most loaded CTA while they
+// lower the maximum.  Every CTA runs its own list heaviest first, so the
+// light blocks fill the gaps at the end.  The order decides only which CTA
+// computes an item, never how.
+struct Schedule {
+  std::vector<uint16_t> off;   // grid + 1 list bounds
+  std::vector<uint16_t> item;  // items, CTA by CTA
+};
+
+// K/V steps of query block mb (two 128-row tiles) in a dense problem: the
+// union of both tiles' key ranges, as the kernel's item decode computes it.
+int dense_block_steps(const PrefillParams& p, int mb) {
+  constexpr int BM = 128, BN = 128;
+  const int m0 = mb * 2 * BM;
+  const int diag = p.top_left ? 0 : p.Lk - p.Lq;
+  int jb = INT_MAX, je = 0;
+  for (int t = 0; t < 2; ++t) {
+    const int mt = m0 + t * BM;
+    if (mt >= p.Lq) continue;
+    const int last = std::min(mt + BM - 1, p.Lq - 1);
+    int kend = p.Lk, kbeg = 0;
+    if (p.win_right >= 0) kend = std::min(p.Lk, last + diag + p.win_right + 1);
+    if (p.win_left >= 0) kbeg = std::max(0, mt + diag - p.win_left);
+    if (kend > kbeg) {
+      jb = std::min(jb, kbeg / BN);
+      je = std::max(je, (kend + BN - 1) / BN);
+    }
+  }
+  return je > jb ? je - jb : 0;
+}
+
+std::shared_ptr<const Schedule> dense_schedule(const PrefillParams& p, int grid) {
+  static std::mutex mu;
+  static std::map<std::array<int, 8>, std::shared_ptr<const Schedule>> cache;
+  const std::array<int, 8> key = {p.B, p.Hq, p.Lq, p.Lk, p.win_left, p.win_right, p.top_left, grid};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto f = cache.find(key);
+    if (f != cache.end()) return f->second;
+  }
+  const int n = p.num_items, nbh = p.B * p.Hq;
+  // Cost in tenths of a K/V step: the steps plus a fixed per-item share of
+  // four steps (the Q load and first S before any PV, the last PV and the
+  // epilogue); of the shares 0, 1.6, 4 and 8 steps, 4 gave the shortest
+  // measured runs over causal and windowed shapes with L 1024 to 8192.
+  std::vector<int> cost(n);
+  for (int i = 0; i < n; ++i) {
+    const int mb = p.num_m_blocks - 1 - i / nbh;  // the kernel's masked item order
+    cost[i] = 10 * dense_block_steps(p, mb) + 40;
+  }
+  std::vector<int> order(n);
+  for (int i = 0; i < n; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+  std::vector<std::vector<int>> bins(grid);
+  std::vector<long> load(grid, 0);
+  for (const int i : order) {
+    const int c = static_cast<int>(std::min_element(load.begin(), load.end()) - load.begin());
+    bins[c].push_back(i);
+    load[c] += cost[i];
+  }
+  for (int iter = 0; iter < 8 * grid; ++iter) {
+    const int hi = static_cast<int>(std::max_element(load.begin(), load.end()) - load.begin());
+    const long top = load[hi];
+    bool moved = false;
+    for (size_t a = 0; a < bins[hi].size() && !moved; ++a) {
+      const int ia = bins[hi][a];
+      for (int c = 0; c < grid && !moved; ++c) {
+        if (c == hi) continue;
+        if (load[c] + cost[ia] < top) {  // a move
+          bins[c].push_back(ia);
+          bins[hi].erase(bins[hi].begin() + a);
+          load[c] += cost[ia];
+          load[hi] -= cost[ia];
+          moved = true;
+          break;
+        }
+        for (size_t b = 0; b < bins[c].size(); ++b) {  // a swap of a heavier for a lighter item
+          const int ib = bins[c][b];
+          const int dlt = cost[ia] - cost[ib];
+          if (dlt > 0 && load[c] + dlt < top) {
+            std::swap(bins[hi][a], bins[c][b]);
+            load[c] += dlt;
+            load[hi] -= dlt;
+            moved = true;
+            break;
+          }
+        }
+      }
+    }
+    if (!moved) break;
+  }
+  auto s = std::make_shared<Schedule>();
+  s->off.assign(grid + 1, 0);
+  std::vector<int> seen(n, 0);
+  for (int c = 0; c < grid; ++c) {
+    std::stable_sort(bins[c].begin(), bins[c].end(), [&](int a, int b) {
+      return cost[a] != cost[b] ? cost[a] > cost[b] : a < b;
+    });
+    for (const int i : bins[c]) {
+      s->item.push_back(static_cast<uint16_t>(i));
+      ++seen[i];
+    }
+    s->off[c + 1] = static_cast<uint16_t>(s->item.size());
+  }
+  for (int i = 0; i < n; ++i)
+    if (seen[i] != 1) return nullptr;  // never launch a schedule that drops or repeats an item
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() >= 64) cache.clear();
+  cache[key] = s;
+  return s;
+}
+
+// Attaches the static schedule to p when the problem fits its bounds; the
+// kernel otherwise keeps the snake order (sched_n = 0).
+void attach_schedule(PrefillParams& p, int grid) {
+  p.sched_n = 0;
+  if (grid > kSchedMaxCtas || p.num_items > kSchedMaxItems || p.num_items <= grid) return;
+  const auto s = dense_schedule(p, grid);
+  if (s == nullptr) return;
+  std::copy(s->off.begin(), s->off.end(), p.sched_off);
+  std::copy(s->item.begin(), s->item.end(), p.sched_item);
+  p.sched_n = p.num_items;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* attn_status_string(attn_status s) {
@@ -361,6 +500,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
   p.num_items = p.num_m_blocks * B * Hq;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
+  if (masked) attach_schedule(p, grid);
   return finish_launch(launch_prefill(p, grid, d, dt, masked, score_xf(p),
                                       static_cast<cudaStream_t>(stream), g_last_name,
                                       sizeof(g_last_name)));

@@ -40,6 +40,11 @@ enum PrefillDt : int { kDtF16 = 0, kDtBF16 = 1, kDtE4M3 = 2 };
 // before masking).
 enum ScoreXf : int { kXfNone = 0, kXfSoftcap = 1, kXfAlibi = 2, kXfBias = 3 };
 
+// Bounds of the host-packed static schedule carried in PrefillParams, chosen
+// so that the launch parameters stay within 4 KB.
+constexpr int kSchedMaxCtas = 160;
+constexpr int kSchedMaxItems = 1536;
+
 // Prefill (dense / varlen) launch parameters.  Tensor maps are 4-D
 // (d, rows, heads, batch); varlen problems use one batch slot and a row base.
 struct PrefillParams {
@@ -80,7 +85,15 @@ struct PrefillParams {
   int page_size, max_pages, num_pages;
   unsigned int* err;
   uint64_t timeout_ns;
+  // Dense masked problems: a static assignment of the work items to CTAs,
+  // packed on the host (sched_n > 0).  CTA c takes items
+  // sched_item[sched_off[c]] .. sched_item[sched_off[c + 1] - 1] in order;
+  // sched_n == 0: the snake order over the plain item list.
+  int sched_n;
+  uint16_t sched_off[kSchedMaxCtas + 1];
+  uint16_t sched_item[kSchedMaxItems];
 };
+static_assert(sizeof(PrefillParams) <= 4096, "prefill launch parameters exceed 4 KB");
 
 // Paged split-KV decode parameters.
 struct DecodeParams {

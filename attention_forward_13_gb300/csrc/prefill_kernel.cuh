@@ -426,8 +426,14 @@ __device__ void order_items(const PrefillParams& p, PrefillSmem<C>& sm) {
 
 // The r-th item of this CTA: rounds of gridDim.x items, alternating direction
 // (snake), so the heavy head of the list is spread evenly across CTAs.
-__device__ __forceinline__ int item_of_round(int r) {
+// With a host-packed schedule, the r-th item of this CTA's list instead
+// (past its end: num_items, which ends every role's loop).
+__device__ __forceinline__ int item_of_round(const PrefillParams& p, int r) {
   const int G = gridDim.x, c = blockIdx.x;
+  if (p.sched_n > 0) {
+    const int pos = p.sched_off[c] + r;
+    return pos < p.sched_off[c + 1] ? static_cast<int>(p.sched_item[pos]) : p.num_items;
+  }
   return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
@@ -500,7 +506,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       int qa[2] = {0, 0};  // arms of each tile's q_full
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int item = item_of_round(r);
+        const int item = item_of_round(p, r);
         if (item >= p.num_items) break;
         PrefillItem it;
         if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it) || it.cnt == 0) continue;
@@ -603,7 +609,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       int oc[2] = {0, 0};  // items finished by each tile so far (o_free phases)
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int item = item_of_round(r);
+        const int item = item_of_round(p, r);
         if (item >= p.num_items) break;
         PrefillItem it;
         if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it) || it.cnt == 0) continue;
@@ -679,7 +685,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       int g = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int item = item_of_round(r);
+        const int item = item_of_round(p, r);
         if (item >= p.num_items) break;
         PrefillItem it;
         if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it) || it.cnt == 0) continue;
@@ -710,7 +716,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
     int pc = 0, oc = 0;
     bool ok = true;
     for (int rr = 0; ok; ++rr) {
-      const int item = item_of_round(rr);
+      const int item = item_of_round(p, rr);
       if (item >= p.num_items) break;
       PrefillItem it;
       if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it)) continue;

@@ -1,10 +1,14 @@
-"""The prefill kernel's work order in group mode and over a paged cache.
+"""The prefill kernel's work order in group mode, over a paged cache, and
+on the host-packed static schedule of dense masked problems.
 
-There the (query block, sequence) slots are sorted by their K/V step count in
-every CTA before any work starts; more than 2048 slots fall back to the plain
+In group mode and over a paged cache the (query block, sequence) slots are
+sorted by their K/V step count in every CTA before any work starts; more than 2048 slots fall back to the plain
 order, and step counts above 254 share the top cost.  The order decides only
 which CTA computes an item, never how, so every case here must match the
 oracle and the per-sequence dense results exactly as any other order would.
+Dense problems with a causal or window mask run each CTA's list from a
+schedule packed on the host (longest processing time first); a lone
+(batch, head) has fewer blocks than CTAs and keeps the plain order.
 
 Composable Kernel FMHA forward page: group mode (seqstart_q / seqstart_k)
 and the paged-KV block table; the sort is this implementation's schedule."""
@@ -94,4 +98,25 @@ def test_paged_chunk_over_a_cache_past_the_top_cost():
         ro, rl = oracle.attn_dense(f64(inp.q[0, r0:r1, h])[None, None], f64(kc[:keep])[None, None],
                                    f64(vc[:keep])[None, None], 1 / math.sqrt(d), True)
         check(o[0, r0:r1, h][None, None], lse[0, h, r0:r1][None, None], ro, rl, f"long seq h{h}")
+    no_device_error()
+
+
+@pytest.mark.parametrize("window,top_left", [(None, False), ((700, 0), False), ((300, 200), True)])
+def test_dense_static_schedule_equals_single_head(window, top_left):
+    """A dense masked problem with more query blocks than CTAs runs on the
+    host-packed static schedule; a single (batch, head) has fewer blocks than
+    CTAs and runs one block per CTA.  Both compute every block the same way,
+    so sampled heads are bit-identical between the two launches."""
+    B, H, L, d = 2, 16, 4096, 128
+    causal = window is None
+    inp = inputs.dense(B, H, H, L, L, d, "bf16", seed=4096, device="cuda", causal=True)
+    o, lse = A.attn_fwd(inp.q, inp.k, inp.v, causal=causal, window=window, top_left=top_left)
+    torch.cuda.synchronize()
+    for b, h in [(0, 0), (1, 7), (1, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        o1, l1 = A.attn_fwd(inp.q[sl].contiguous(), inp.k[sl].contiguous(), inp.v[sl].contiguous(),
+                            causal=causal, window=window, top_left=top_left)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o[sl]), f"b{b} h{h}"
+        assert torch.equal(l1, lse[sl]), f"b{b} h{h} LSE"
     no_device_error()
