@@ -187,37 +187,46 @@ __device__ __forceinline__ void widen_v_tile(const uint8_t* raw, uint8_t* out, i
   }
 }
 
-// Adds inv_scale * bias[c] to the raw scores s[c], c < min(128, nvalid)
-// (columns past the key end are masked afterwards).  Whole 16-byte loads
-// where the 8 keys exist, element loads at the ragged end.
-template <bool BF16>
-__device__ __forceinline__ void add_bias_row(float* s, const void* src, int nvalid,
-                                             float inv_scale) {
-  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  const T* b = reinterpret_cast<const T*>(src);
+// Elementwise bias (Composable Kernel bias kargs).  One row's segment for a
+// K/V tile (128 keys) is loaded into registers a step ahead, raw: 16-byte
+// loads where all 8 keys are valid, element loads at the tail (keys past the
+// end read as 0; they are masked later).
+__device__ __forceinline__ void load_bias_regs(uint4 (&bn)[16], const void* src, int nvalid) {
+  const uint16_t* b = reinterpret_cast<const uint16_t*>(src);
 #pragma unroll
   for (int c8 = 0; c8 < 16; ++c8) {
     if (8 * c8 + 8 <= nvalid) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(b + 8 * c8));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float lo, hi;
-        if constexpr (BF16) {
-          lo = __uint_as_float(w[i] << 16);
-          hi = __uint_as_float(w[i] & 0xffff0000u);
-        } else {
-          const __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
-          lo = __low2float(h2);
-          hi = __high2float(h2);
-        }
-        s[8 * c8 + 2 * i] = fmaf(lo, inv_scale, s[8 * c8 + 2 * i]);
-        s[8 * c8 + 2 * i + 1] = fmaf(hi, inv_scale, s[8 * c8 + 2 * i + 1]);
-      }
+      bn[c8] = __ldg(reinterpret_cast<const uint4*>(b + 8 * c8));
     } else {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (8 * c8 + i < nvalid) s[8 * c8 + i] = fmaf(static_cast<float>(b[8 * c8 + i]), inv_scale, s[8 * c8 + i]);
+        if (8 * c8 + i < nvalid) w[i >> 1] |= static_cast<uint32_t>(__ldg(b + 8 * c8 + i)) << (16 * (i & 1));
+      bn[c8] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// Adds 32 bias values (natural-log units, so divided by the scale folded in
+// later) to 32 raw scores.
+template <bool BF16>
+__device__ __forceinline__ void add_bias_quarter(float* s, const uint4* bn, float inv_scale) {
+#pragma unroll
+  for (int c8 = 0; c8 < 4; ++c8) {
+    const uint32_t w[4] = {bn[c8].x, bn[c8].y, bn[c8].z, bn[c8].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float lo, hi;
+      if constexpr (BF16) {
+        lo = __uint_as_float(w[i] << 16);
+        hi = __uint_as_float(w[i] & 0xffff0000u);
+      } else {
+        const __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
+        lo = __low2float(h2);
+        hi = __high2float(h2);
+      }
+      s[8 * c8 + 2 * i] = fmaf(lo, inv_scale, s[8 * c8 + 2 * i]);
+      s[8 * c8 + 2 * i + 1] = fmaf(hi, inv_scale, s[8 * c8 + 2 * i + 1]);
     }
   }
 }
@@ -735,6 +744,24 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
 
       float m_use = -INFINITY;  // exp2 subtrahend currently in use (log2 units)
       float l = 0.0f;           // running denominator w.r.t. m_use
+      // Bias: this row's segment for the coming K/V tile, loaded right after
+      // the previous step's P is handed over, so that the loads run while the
+      // tensor core computes the next S; the L2 is warmed one step further
+      // ahead (the valid bytes only: up to three 128-byte lines).
+      uint4 bn[16];
+      auto fetch_bias = [&](int jj) {  // registers for step jj, L2 for step jj + 1
+        const int k0 = (it.jb + it.ub[t] + jj) * C::BN;
+        load_bias_regs(bn, bias_row + k0, it.Lk - k0);
+        if (jj + 1 < nt) {
+          const char* nb = reinterpret_cast<const char*>(bias_row + k0 + C::BN);
+          const int bytes = min(it.Lk - (k0 + C::BN), C::BN) * static_cast<int>(sizeof(T));
+          prefetch_l2(nb);
+          if (bytes > 128) prefetch_l2(nb + 128);
+          prefetch_l2(nb + bytes - 1);
+        }
+      };
+      if constexpr (XF == kXfBias)
+        if (qi < it.Lq && nt > 0) fetch_bias(0);
       for (int j = 0; j < nt; ++j) {
         ok = __all_sync(0xffffffffu, w.wait(&sm.s_full[t], pc & 1, kErrPrefillSFull));
         if (!ok) break;
@@ -746,12 +773,34 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           uint32_t (&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
           uint32_t (&a2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
           uint32_t (&a3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
-          tmem_ld32(tS + 0, a0);
-          tmem_ld32(tS + 32, a1);
-          tmem_ld32(tS + 64, a2);
-          tmem_ld32(tS + 96, a3);
-          tmem_ld_wait();
-          reg_fence(sr);
+          if constexpr (XF == kXfBias) {
+            // A quarter of the scores at a time, each taking its bias from
+            // registers as it lands, so that the prefetched segment and the
+            // scores are never all live at once.
+            tmem_ld32(tS + 0, a0);
+            tmem_ld_wait();
+            reg_fence(a0);
+            if (qi < it.Lq) add_bias_quarter<BF16>(reinterpret_cast<float*>(&sr[0]), &bn[0], p.inv_scale);
+            tmem_ld32(tS + 32, a1);
+            tmem_ld_wait();
+            reg_fence(a1);
+            if (qi < it.Lq) add_bias_quarter<BF16>(reinterpret_cast<float*>(&sr[32]), &bn[4], p.inv_scale);
+            tmem_ld32(tS + 64, a2);
+            tmem_ld_wait();
+            reg_fence(a2);
+            if (qi < it.Lq) add_bias_quarter<BF16>(reinterpret_cast<float*>(&sr[64]), &bn[8], p.inv_scale);
+            tmem_ld32(tS + 96, a3);
+            tmem_ld_wait();
+            reg_fence(a3);
+            if (qi < it.Lq) add_bias_quarter<BF16>(reinterpret_cast<float*>(&sr[96]), &bn[12], p.inv_scale);
+          } else {
+            tmem_ld32(tS + 0, a0);
+            tmem_ld32(tS + 32, a1);
+            tmem_ld32(tS + 64, a2);
+            tmem_ld32(tS + 96, a3);
+            tmem_ld_wait();
+            reg_fence(sr);
+          }
         }
         // Raw scores in place; the soft-cap variant turns them into tanh
         // values whose log2-unit score is cap*log2(e)*s, else scale*log2(e)
@@ -789,19 +838,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           }
         } else if constexpr (XF == kXfBias) {
           // CK elementwise bias (natural-log units, added to the scaled score).
-          if (qi < it.Lq) {
-            add_bias_row<BF16>(s, bias_row + j0, it.Lk - j0, p.inv_scale);
-            // Warm L2 with this row's bias for the next K/V tile (its valid
-            // bytes only: up to three 128-byte lines), so that next step's
-            // loads wait less.
-            if (j + 1 < nt) {
-              const char* nb = reinterpret_cast<const char*>(bias_row + j0 + C::BN);
-              const int bytes = min(it.Lk - (j0 + C::BN), C::BN) * static_cast<int>(sizeof(T));
-              prefetch_l2(nb);
-              if (bytes > 128) prefetch_l2(nb + 128);
-              prefetch_l2(nb + bytes - 1);
-            }
-          }
+          // Composable Kernel elementwise bias (natural-log units, added to the
+          // scaled score): added above, as the scores left tensor memory.
         }
         if ((j0 + C::BN > it.Lk) ||
             (MASK && p.win_right >= 0 && j0 + C::BN - 1 > mt + diag + p.win_right) ||
@@ -851,6 +889,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full[t]);
+        if constexpr (XF == kXfBias)
+          if (qi < it.Lq && j + 1 < nt) fetch_bias(j + 1);
       }
       if (!ok) break;
 
