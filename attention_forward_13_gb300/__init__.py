@@ -22,7 +22,7 @@ from . import _lib
 __all__ = ["attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_splitkv_combine",
            "attn_paged_workspace_bytes", "attn_paged_auto_splits", "attn_device_error",
            "attn_selftest_timeout", "attn_last_kernel_name", "attn_paged_window_pages",
-           "attn_fwd_paged_noalloc", "AttnError", "library"]
+           "attn_fwd_paged_noalloc", "attn_dense_schedule", "AttnError", "library"]
 
 
 class AttnError(RuntimeError):
@@ -200,6 +200,21 @@ def attn_paged_window_pages(Lq, page_size, max_pages_per_seq, window=None, causa
     opts = _opts(None, causal, 0.0, None, window, top_left)
     return int(library().attn_paged_window_pages(Lq, page_size, max_pages_per_seq,
                                                  ctypes.byref(opts)))
+
+
+def attn_dense_schedule(B, Hq, Lq, Lk, grid, causal=False, window=None, top_left=False):
+    """The static schedule attn_fwd runs on `grid` CTAs for a dense masked
+    problem: a list of `grid` lists of work items (CTA by CTA, in run order),
+    or None where the problem keeps the plain snake order."""
+    opts = _opts(None, causal, 0.0, None, window, top_left)
+    n = B * Hq * ((Lq + 255) // 256) if Lq > 0 else 0
+    off = (ctypes.c_int32 * (max(grid, 0) + 1))()
+    item = (ctypes.c_int32 * max(n, 1))()
+    st = library().attn_dense_schedule(B, Hq, Lq, Lk, ctypes.byref(opts), grid, off, item)
+    if st == 2:
+        return None
+    _check(st, "attn_dense_schedule")
+    return [list(item[off[c]:off[c + 1]]) for c in range(grid)]
 
 
 def attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, num_splits=0, o=None, lse=True,

@@ -33,7 +33,7 @@ ATTN_F16, ATTN_BF16, ATTN_E4M3 = 0, 1, 2
 EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_splitkv_combine",
            "attn_paged_workspace_bytes", "attn_paged_auto_splits", "attn_status_string",
            "attn_last_kernel_name", "attn_device_error", "attn_selftest_timeout",
-           "attn_fwd_paged_noalloc", "attn_paged_window_pages")
+           "attn_fwd_paged_noalloc", "attn_paged_window_pages", "attn_dense_schedule")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
@@ -60,6 +60,9 @@ def _declare(lib):
     lib.attn_paged_auto_splits.restype = _I
     lib.attn_paged_window_pages.argtypes = [_I, _I, _I, O]
     lib.attn_paged_window_pages.restype = _I
+    IP = ctypes.POINTER(ctypes.c_int32)
+    lib.attn_dense_schedule.argtypes = [_I, _I, _I, _I, O, _I, IP, IP]
+    lib.attn_dense_schedule.restype = _I
     lib.attn_status_string.argtypes = [_I]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_last_kernel_name.argtypes = []

@@ -366,11 +366,20 @@ std::shared_ptr<const Schedule> dense_schedule(const PrefillParams& p, int grid)
   return s;
 }
 
-// Attaches the static schedule to p when the problem fits its bounds; the
-// kernel otherwise keeps the snake order (sched_n = 0).
+// Whether a dense problem runs on the static schedule: a causal or window
+// mask, within the bounds the launch parameters carry, and more work items
+// than CTAs (else every CTA has at most one item and the order is moot).
+bool schedule_applies(const PrefillParams& p, int grid) {
+  const bool masked = p.win_left >= 0 || p.win_right >= 0;
+  return masked && grid > 0 && grid <= kSchedMaxCtas && p.num_items <= kSchedMaxItems &&
+         p.num_items > grid;
+}
+
+// Attaches the static schedule to p when it applies; the kernel otherwise
+// keeps the snake order (sched_n = 0).
 void attach_schedule(PrefillParams& p, int grid) {
   p.sched_n = 0;
-  if (grid > kSchedMaxCtas || p.num_items > kSchedMaxItems || p.num_items <= grid) return;
+  if (!schedule_applies(p, grid)) return;
   const auto s = dense_schedule(p, grid);
   if (s == nullptr) return;
   std::copy(s->off.begin(), s->off.end(), p.sched_off);
@@ -500,7 +509,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
   p.num_items = p.num_m_blocks * B * Hq;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
-  if (masked) attach_schedule(p, grid);
+  attach_schedule(p, grid);
   return finish_launch(launch_prefill(p, grid, d, dt, masked, score_xf(p),
                                       static_cast<cudaStream_t>(stream), g_last_name,
                                       sizeof(g_last_name)));
@@ -657,6 +666,30 @@ size_t attn_paged_workspace_bytes(int B, int Lq, int Hq, int d, int num_splits) 
   if (B <= 0 || Lq <= 0 || Hq <= 0 || d <= 0 || num_splits <= 1) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * Lq;
   return static_cast<size_t>(num_splits) * rows * (static_cast<size_t>(d) + 1) * sizeof(float);
+}
+
+attn_status attn_dense_schedule(int B, int Hq, int Lq, int Lk, const attn_opts* opts, int grid,
+                                int32_t* off, int32_t* item) {
+  if (B <= 0 || Hq <= 0 || Lq <= 0 || Lk < 0 || grid <= 0 || off == nullptr || item == nullptr)
+    return ATTN_ERR_INVALID;
+  const int64_t n = static_cast<int64_t>((Lq + 255) / 256) * B * Hq;
+  if (n > kSchedMaxItems) return ATTN_ERR_UNSUPPORTED;
+  PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.Hq = Hq;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  resolve_window(opts, &p.win_left, &p.win_right);
+  p.top_left = (opts != nullptr && opts->top_left) ? 1 : 0;
+  p.num_m_blocks = (Lq + 255) / 256;
+  p.num_items = static_cast<int>(n);
+  if (!schedule_applies(p, grid)) return ATTN_ERR_UNSUPPORTED;
+  const auto s = dense_schedule(p, grid);
+  if (s == nullptr) return ATTN_ERR_INVALID;
+  for (int c = 0; c <= grid; ++c) off[c] = s->off[c];
+  for (int i = 0; i < p.num_items; ++i) item[i] = s->item[i];
+  return ATTN_OK;
 }
 
 int attn_paged_window_pages(int Lq, int page_size, int max_pages_per_seq, const attn_opts* opts) {

@@ -240,6 +240,25 @@ int attn_paged_auto_splits(int B, int Hkv, int max_pages_per_seq);
  * opts may be NULL. */
 int attn_paged_window_pages(int Lq, int page_size, int max_pages_per_seq, const attn_opts* opts);
 
+/* The static work schedule attn_fwd runs for a dense problem with a causal
+ * or window mask on a grid of `grid` CTAs (a load-balancing order of this
+ * implementation; the pages fix none).  Work item i is query block
+ * ceil(Lq/256) - 1 - i / (B*Hq) (256 rows) of batch (i % (B*Hq)) / Hq and
+ * head i % Hq; CTA c runs items item[off[c]] .. item[off[c+1] - 1] in that
+ * order.  The items are packed longest processing time first (cost: the
+ * block's K/V tiles of 128 keys plus 4), then moved and swapped off the
+ * most loaded CTA while that lowers its load; each CTA's list runs heaviest
+ * first.  attn_fwd launches min(SM count, items) CTAs and uses this
+ * schedule exactly when this call returns ATTN_OK for that grid.
+ *   off: host int32 [grid + 1]; item: host int32 [B * Hq * ceil(Lq / 256)].
+ *   Returns ATTN_ERR_UNSUPPORTED when the problem keeps the plain snake
+ *   order (no mask, more than 1536 items or 160 CTAs, or no more items than
+ *   CTAs), ATTN_ERR_INVALID for non-positive sizes or NULL buffers.  Host
+ *   only: needs no device.  opts as for attn_fwd (only the mask fields are
+ *   read); may be NULL. */
+attn_status attn_dense_schedule(int B, int Hq, int Lq, int Lk, const attn_opts* opts, int grid,
+                                int32_t* off, int32_t* item);
+
 /* Human-readable name of a status. */
 const char* attn_status_string(attn_status status);
 
