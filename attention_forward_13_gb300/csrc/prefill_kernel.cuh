@@ -14,11 +14,12 @@
 // fold).  The Blackwell design here differs from all three:
 //
 //  * persistent: one CTA per SM walks a list of work items (a 256-row query
-//    block of one (batch, head)) in snake order across CTAs: heaviest causal
-//    blocks first for dense problems; in group mode and over a paged cache
-//    every CTA first sorts the (query block, sequence) pairs by cost.  The
-//    next item's Q load and its first S = Q K^T overlap the current item's
-//    last P.V and epilogue.
+//    block of one (batch, head)): dense masked problems run the per-CTA
+//    lists the host packed for the shape (longest processing time first),
+//    other dense problems a snake order across CTAs; in group mode and over
+//    a paged cache every CTA first sorts the (query block, sequence) pairs
+//    by cost.  The next item's Q load and its first S = Q K^T overlap the
+//    current item's last P.V and epilogue.
 //  * each item is two 128-row query tiles sharing every 128-key K/V tile;
 //    warps 0-3 run the softmax of tile 0, warps 4-7 that of tile 1, warp 8
 //    issues TMA, warp 9 issues tcgen05.mma (the whole warp runs the loop, one
