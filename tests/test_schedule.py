@@ -4,7 +4,7 @@ The schedule decides only which CTA runs which work item (a 256-row query
 block of one (batch, head)), never how an item is computed; GPU tests check
 that outputs do not depend on it.  Here, on the CPU, its host logic is
 checked against what its contract states: every item exactly once, each
-CTA's list heaviest first, and a makespan within the list-scheduling bound
+CTA's list lightest first, and a makespan within the list-scheduling bound
 (mean load + the largest item) and no worse than the plain snake order.
 Item costs are recomputed by brute force from the mask definition (a key
 tile counts when some (row, key) pair of the block keeps it; Composable
@@ -90,7 +90,7 @@ def test_schedule_contract(shape):
     assert sorted(flat) == list(range(n)), "every work item exactly once"
     for lst in sched:
         cl = [cost[i] for i in lst]
-        assert cl == sorted(cl, reverse=True), "each CTA's list runs heaviest first"
+        assert cl == sorted(cl), "each CTA's list runs lightest first"
     loads = [sum(cost[i] for i in lst) for lst in sched]
     assert max(loads) <= sum(cost) / GRID + max(cost), "list-scheduling bound"
     assert max(loads) <= max(snake_loads(cost, GRID)), "no worse than the snake order"
