@@ -120,3 +120,25 @@ def test_dense_static_schedule_equals_single_head(window, top_left):
         assert torch.equal(o1, o[sl]), f"b{b} h{h}"
         assert torch.equal(l1, lse[sl]), f"b{b} h{h} LSE"
     no_device_error()
+
+
+def test_dense_schedule_with_keyless_blocks():
+    """Lq 3000 > Lk 1000, causal (bottom-right): rows below 2000 keep no key,
+    so most query blocks cost only their fixed share; the 768 blocks of
+    4 x 16 heads run on the static schedule.  Keyless rows give O = 0 and
+    LSE = -inf; the other rows of sampled heads match the oracle."""
+    B, H, Lq, Lk, d = 4, 16, 3000, 1000, 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert A.attn_dense_schedule(B, H, Lq, Lk, min(sms, 768), causal=True) is not None
+    inp = inputs.dense(B, H, H, Lq, Lk, d, "bf16", seed=3000, device="cuda", causal=True)
+    o, lse = A.attn_fwd(inp.q, inp.k, inp.v, causal=True)
+    torch.cuda.synchronize()
+    cut = Lq - Lk
+    assert torch.all(o[:, :, :cut] == 0)
+    assert torch.all(torch.isneginf(lse[:, :, :cut]))
+    for b, h in [(0, 0), (1, 7), (3, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ro, rl = oracle.attn_dense(f64(inp.q[sl][:, :, cut:]), f64(inp.k[sl]), f64(inp.v[sl]),
+                                   1 / math.sqrt(d), True)
+        check(o[sl][:, :, cut:], lse[sl][:, :, cut:], ro, rl, f"keyless blocks b{b} h{h}")
+    no_device_error()
