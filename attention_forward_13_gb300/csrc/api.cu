@@ -131,6 +131,9 @@ void resolve_window(const attn_opts* opts, int* wl, int* wr) {
   if (opts->causal) *wr = 0;  // any window_right >= 0 is looser than causal
 }
 
+// 256-row query blocks of L rows (no int overflow for any L >= 0).
+int m_blocks(int L) { return static_cast<int>((static_cast<int64_t>(L) + 255) / 256); }
+
 void fill_common(PrefillParams& p, const attn_opts* opts, int d) {
   const float scale = resolve_scale(opts, d);
   p.scale = scale;
@@ -457,7 +460,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     const attn_status so_ = check_opts(opts, Hq, true);
     if (so_ != ATTN_OK) return so_;
   }
-  if (static_cast<int64_t>(B) * Hq * ((Lq + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * Hq * m_blocks(Lq) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
 
   PrefillParams p;
   memset(&p, 0, sizeof(p));
@@ -498,7 +501,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.Hkv = Hkv;
   p.Lq = Lq;
   p.Lk = Lk;
-  p.num_m_blocks = (Lq + 255) / 256;
+  p.num_m_blocks = m_blocks(Lq);
   p.err = err;
   fill_common(p, opts, d);
   if (opts != nullptr && opts->bias != nullptr) {
@@ -540,7 +543,7 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
     return ATTN_ERR_INVALID;
   for (const attn_strides* s : {&sq, &sk, &sv, &so})
     if (!stride_ok(s->row, eb) || !stride_ok(s->head, eb)) return ATTN_ERR_INVALID;
-  if (static_cast<int64_t>(B) * Hq * ((max_seqlen_q + 255) / 256) > 0x7fffffffLL)
+  if (static_cast<int64_t>(B) * Hq * m_blocks(max_seqlen_q) > 0x7fffffffLL)
     return ATTN_ERR_UNSUPPORTED;
   {
     const attn_status so_ = check_opts(opts, Hq, false);
@@ -591,7 +594,7 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   p.Hkv = Hkv;
   p.Lq = 0;
   p.Lk = 0;
-  p.num_m_blocks = (max_seqlen_q + 255) / 256;
+  p.num_m_blocks = m_blocks(max_seqlen_q);
   p.err = err;
   fill_common(p, opts, d);
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
@@ -614,7 +617,7 @@ attn_status paged_prefill(const void* q, const void* k_pool, const void* v_pool,
                           float* lse, int B, int Lq, int Hq, int Hkv, int d, bool bf16,
                           int page_size, int num_pages, int max_pages, const attn_opts* opts,
                           cudaStream_t stream) {
-  if (static_cast<int64_t>(B) * Hq * ((Lq + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * Hq * m_blocks(Lq) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   PrefillParams p;
   memset(&p, 0, sizeof(p));
   unsigned int* err = nullptr;
@@ -645,7 +648,7 @@ attn_status paged_prefill(const void* q, const void* k_pool, const void* v_pool,
   p.Hkv = Hkv;
   p.Lq = Lq;
   p.Lk = max_pages * page_size;
-  p.num_m_blocks = (Lq + 255) / 256;
+  p.num_m_blocks = m_blocks(Lq);
   p.err = err;
   fill_common(p, opts, d);
   p.block_table = block_table;
@@ -673,7 +676,7 @@ attn_status attn_dense_schedule(int B, int Hq, int Lq, int Lk, const attn_opts* 
                                 int32_t* off, int32_t* item) {
   if (B <= 0 || Hq <= 0 || Lq <= 0 || Lk < 0 || grid <= 0 || off == nullptr || item == nullptr)
     return ATTN_ERR_INVALID;
-  const int64_t n = static_cast<int64_t>((Lq + 255) / 256) * B * Hq;
+  const int64_t n = static_cast<int64_t>(m_blocks(Lq)) * B * Hq;
   if (n > kSchedMaxItems) return ATTN_ERR_UNSUPPORTED;
   PrefillParams p;
   memset(&p, 0, sizeof(p));
@@ -683,7 +686,7 @@ attn_status attn_dense_schedule(int B, int Hq, int Lq, int Lk, const attn_opts* 
   p.Lk = Lk;
   resolve_window(opts, &p.win_left, &p.win_right);
   p.top_left = (opts != nullptr && opts->top_left) ? 1 : 0;
-  p.num_m_blocks = (Lq + 255) / 256;
+  p.num_m_blocks = m_blocks(Lq);
   p.num_items = static_cast<int>(n);
   if (!schedule_applies(p, grid)) return ATTN_ERR_UNSUPPORTED;
   const auto s = dense_schedule(p, grid);

@@ -124,3 +124,9 @@ def test_schedule_not_used(args, kw):
 def test_schedule_rejects_bad_sizes(args):
     with pytest.raises(A.AttnError):
         A.attn_dense_schedule(*args, causal=True)
+
+
+def test_schedule_query_block_count_does_not_overflow():
+    """Lq near 2^31: the block count is taken in 64 bits, so the problem is
+    simply too large for the static schedule (no wrapped-around count)."""
+    assert A.attn_dense_schedule(1, 1, 2 ** 31 - 10, 100, GRID, causal=True) is None
