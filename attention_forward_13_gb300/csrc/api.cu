@@ -31,7 +31,7 @@ unsigned int* g_err_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
 std::mutex g_mu;
 
-thread_local char g_last_name[160] = "";
+thread_local char g_last_name[256] = "";
 
 // Default limit of every in-kernel wait: generous for any legal schedule, and
 // still a bounded time if a schedule is ever wrong.
@@ -836,8 +836,16 @@ attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool
   attn_status st1 = finish_launch(launch_decode(p, d, bf16, p.softcap > 0.0f, Lq * (Hq / Hkv), s,
                                                 g_last_name, sizeof(g_last_name)));
   if (st1 != ATTN_OK || num_splits == 1) return st1;
-  return attn_splitkv_combine(o_partial, p.lse_part, num_splits, B, Hq, Lq, d, p.sink, o, dtype,
-                              lse, stream);
+  char decode_name[sizeof(g_last_name)];
+  memcpy(decode_name, g_last_name, sizeof(decode_name));
+  const attn_status st2 = attn_splitkv_combine(o_partial, p.lse_part, num_splits, B, Hq, Lq, d,
+                                               p.sink, o, dtype, lse, stream);
+  if (st2 == ATTN_OK) {  // both kernels of the call, in launch order
+    char both[sizeof(g_last_name)];
+    snprintf(both, sizeof(both), "%s+%s", decode_name, g_last_name);
+    memcpy(g_last_name, both, sizeof(both));
+  }
+  return st2;
 }
 
 }  // extern "C"

@@ -67,6 +67,12 @@ extern "C" attn_status attn_fwd_paged_noalloc(const void* q, const void* k_pool,
       max_pages_per_seq <= 0 || Hkv <= 0)
     return ATTN_ERR_INVALID;
   if (B == 0 || Lq == 0) return ATTN_OK;
+  // Chunks of more than 16 query rows per kv head run the prefill kernel,
+  // which ignores num_splits and uses no scratch: nothing to check or lower.
+  if (Hq % Hkv == 0 && static_cast<int64_t>(Lq) * (Hq / Hkv) > 16)
+    return attn_fwd_paged(q, k_pool, v_pool, block_table, seqlens_k, o, lse, B, Lq, Hq, Hkv, d,
+                          dtype, page_size, num_pages, max_pages_per_seq, 1, nullptr, nullptr,
+                          opts, stream);
   // Split count: an explicit count must fit the scratch; the automatic choice
   // is lowered until it fits (one split needs no scratch at all).
   if (num_splits == 0) {

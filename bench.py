@@ -1,20 +1,26 @@
 #!/usr/bin/env python
 """Benchmark of the fused attention forward on GB300.
 
-Default (one GPU): the dense causal prefill workload B4 H16 L2048 d128 bf16,
-metric = attention-forward TFLOP/s on unmasked (query, key) pairs.  The same
-run also measures the other full-size workloads (GQA long prefill, paged
-decode in GB/s, varlen softcap+sink prefill) and reports them under "extra".
+Default (one GPU): the GQA causal long prefill B2 Hq32 Hkv8 L8192 d128 bf16
+(the largest single-GPU workload; 4 query heads per kv head), metric =
+attention-forward TFLOP/s on unmasked (query, key) pairs.  The same run also
+measures the other full-size workloads (dense causal prefill B4 H16 L2048,
+paged decode in GB/s, varlen soft-cap + sink prefill, the masks, chunked
+prefill, FP8) and reports them under "extra".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Timing: W untimed warm-up steps, then K steps; before every step a 256 MiB
-buffer is written so L2 (129 MB) holds nothing of the inputs; each step's
-kernels are bracketed by CUDA events recorded on the launching stream; the
-timed loop is bracketed by a barrier and a device synchronise.  nvidia-smi
-clocks are sampled during the timed loop.  Multi-GPU (torchrun): every rank
-runs its own independent batch (weak scaling, no data-path collective); the
-reported value is the sum of the work over the max time over ranks.
+Timing: W untimed warm-up steps, then K timed steps.  A step is `passes`
+back-to-back passes of the whole hot path over the workload (each pass one
+call of the public entry point on inputs resident in HBM), enough passes that
+the timed loop lasts about --min-seconds of wall time so the clocks are
+sampled under load.  Before every pass a 256 MiB buffer is written so L2
+(129 MB) holds nothing of the inputs; each pass is bracketed by CUDA events
+recorded on the launching stream (the flush lies outside them); the timed
+loop is bracketed by a barrier and a device synchronise.  nvidia-smi clocks
+are sampled during the timed loop.  Multi-GPU (torchrun): every rank runs its
+own independent batch (weak scaling, no data-path collective); the reported
+value is the sum of the work over the max time over ranks.
 --impl reference times the fp64 CPU oracle (the only reference this project
 has: the pages ship no runnable code) on a bounded sample of the workload.
 """
@@ -206,8 +212,10 @@ def aggregate(work_local: float, ms_local: float, world: int):
 
 
 # ---------------------------------------------------------------------------
-def time_steps(fn, steps, warmup, stream, flush):
-    """W untimed steps, then K steps with a flush before each and events around fn."""
+def time_steps(fn, steps, warmup, stream, flush, passes=1):
+    """W untimed steps, then K steps of `passes` passes; before every pass a
+    flush, around every pass a pair of events.  Returns the device time of
+    each step (the sum of its passes) in ms."""
     import torch
     for _ in range(warmup):
         flush()
@@ -215,15 +223,18 @@ def time_steps(fn, steps, warmup, stream, flush):
     torch.cuda.synchronize()
     evs = []
     for _ in range(steps):
-        flush()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        fn()
-        b.record(stream)
-        evs.append((a, b))
+        step = []
+        for _ in range(passes):
+            flush()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            step.append((a, b))
+        evs.append(step)
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in evs]
+    return [sum(a.elapsed_time(b) for a, b in step) for step in evs]
 
 
 def make_flush():
@@ -245,31 +256,44 @@ def run_ours(args, rank, world, local):
     flush = make_flush()
     dev = "cuda"
 
-    # ---- headline: dense causal prefill B4 H16 L2048 d128 bf16 ---------------
-    B, H, L, d = 4, 16, 2048, 128
-    inp = inputs.dense(B, H, H, L, L, d, "bf16", seed=1002 + 1000 * rank, device=dev,
+    # ---- headline: GQA causal prefill B2 Hq32 Hkv8 L8192 d128 bf16 -----------
+    B, Hq, Hkv, L, d = 2, 32, 8, 8192, 128
+    inp = inputs.dense(B, Hq, Hkv, L, L, d, "bf16", seed=1003 + 1000 * rank, device=dev,
                        causal=True)
     o = torch.empty_like(inp.q)
-    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
-    flops = dense_flops(B, H, L, L, d, True)
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=dev)
+    flops = dense_flops(B, Hq, L, L, d, True)
 
     def step():
         A.attn_fwd(inp.q, inp.k, inp.v, o=o, lse=lse, causal=True)
 
+    walls = []
+    for _ in range(args.warmup):
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step()
+        torch.cuda.synchronize()
+        walls.append(time.perf_counter() - t0)
+    # passes per step from the warm-up passes (the first one pays the set-up)
+    per = statistics.median(walls[1:] or walls) + 5e-5  # + the flush
+    passes = args.passes or max(1, int(math.ceil(args.min_seconds / (per * args.steps))))
     barrier(world)
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     wall0 = time.perf_counter()
-    times = time_steps(step, args.steps, args.warmup, stream, flush)
+    times = time_steps(step, args.steps, 0, stream, flush, passes)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
-    ms = statistics.mean(times)
-    total_flops, ms_max = aggregate(flops, ms, world)
+    kernel = A.attn_last_kernel_name()
+    ms = statistics.mean(times)  # one step = `passes` passes
+    total_flops, ms_max = aggregate(flops * passes, ms, world)
     tflops = total_flops / (ms_max * 1e-3) / 1e12
-    kern_tflops = flops / (ms * 1e-3) / 1e12
+    ms_pass = ms / passes
+    kern_tflops = flops / (ms_pass * 1e-3) / 1e12
 
     # ---- e2e through the public API with host buffers ------------------------
     hq = inp.q.cpu().pin_memory()
@@ -292,6 +316,7 @@ def run_ours(args, rank, world, local):
     e2e_flops, e2e_ms_max = aggregate(flops, e2e_ms, world)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    del hq, hk, hv, ho, hl, dq, dk, dv
 
     result = {
         "metric": "attn fwd TFLOPS (causal prefill, unmasked pairs) & % of GB300 bf16 tensor peak",
@@ -306,25 +331,29 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), bf16)",
-        "config": {"workload": "dense causal prefill B4 H16 L2048 d128 bf16 (bottom-right causal)",
-                   "B": B, "H": H, "seq_len": L, "head_dim": d, "causal": True,
+        "config": {"workload": "GQA causal prefill B2 Hq32 Hkv8 L8192 d128 bf16 (bottom-right causal)",
+                   "B": B, "Hq": Hq, "Hkv": Hkv, "seq_len": L, "head_dim": d, "causal": True,
+                   "passes_per_step": passes, "ms_per_pass": round(ms_pass, 4),
                    "parallelism": f"independent batch per GPU x{world}",
-                   "l2": "256 MiB buffer written before every step (flush)"},
+                   "l2": "256 MiB buffer written before every pass (flush), outside the events"},
         "roofline": {"bound": "tensor", "achieved": round(kern_tflops, 2),
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(kern_tflops / pk["bf16_tflops"], 4),
-                     "traffic": traffic_for("prefill_B4H16L2048d128_causal", "prefill_kernel.cuh"),
+                     "traffic": traffic_for("prefill_gqa_B2Hq32Hkv8L8192d128_causal",
+                                            "prefill_kernel.cuh"),
                      "peak_source": f"{pk_src} bf16 burst (MEASURED_PEAKS.json)"
                      if pk_src == "measured" else "fallback 1.9 PFLOP/s",
-                     "kernel": A.attn_last_kernel_name(),
+                     "kernel": kernel,
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": round(e2e_flops / (e2e_ms_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms_max, 4)},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * passes,
         "clocks": clocks,
         "wall_s_timed_loop": round(wall, 3),
     }
+    del inp, o, lse
+    torch.cuda.empty_cache()
     if A.attn_device_error() != 0:
         result["device_error"] = True
 
@@ -343,8 +372,10 @@ def run_extra(args, rank, pk, stream, flush, only=None):
     steps = max(3, args.steps // 2) if only is None else args.steps
     warm = 3 if only is None else args.warmup
     out = {}
-    if only in (None, "gqa"):
+    if only == "gqa":  # the headline workload alone (profiling)
         out.update(_extra_gqa(A, inputs, pk, stream, flush, steps, warm))
+    if only in (None, "dense"):
+        out.update(_extra_dense(A, inputs, pk, stream, flush, steps, warm))
     if only in (None, "decode"):
         out.update(_extra_decode(A, inputs, pk, stream, flush, steps, warm, args.decode_batch))
     if only in (None, "varlen"):
@@ -359,7 +390,8 @@ def run_extra(args, rank, pk, stream, flush, only=None):
 
 
 def _extra_fp8(A, inputs, pk, stream, flush, steps, warm):
-    """FP8 static quantisation on the headline shape (e4m3 Q/K/V/O, causal).
+    """FP8 static quantisation on the dense B4 H16 L2048 d128 shape (e4m3
+    Q/K/V/O, causal).
     Roofline peak: S = Q K^T runs on the e4m3 tensor path (2x the bf16 rate,
     nominal ratio) and P.V on the fp16 path, half of the FLOPs each, so the
     peak is the measured bf16 peak x 4/3."""
@@ -408,8 +440,8 @@ def _tensor_entry(fl, ms, pk, kernel, **extra):
 
 
 def _extra_masks(A, inputs, pk, stream, flush, steps, warm):
-    """The sliding-window, ALiBi and elementwise-bias variants on the headline
-    shape (FLOPs count kept pairs only)."""
+    """The sliding-window, ALiBi and elementwise-bias variants on the dense
+    B4 H16 L2048 d128 shape (FLOPs count kept pairs only)."""
     import torch
     out = {}
     B, H, L, d = 4, 16, 2048, 128
@@ -442,6 +474,21 @@ def _extra_masks(A, inputs, pk, stream, flush, steps, warm):
     return out
 
 
+def _extra_dense(A, inputs, pk, stream, flush, steps, warm):
+    """Dense causal prefill B4 H16 L2048 d128 bf16."""
+    import torch
+    B, H, L, d = 4, 16, 2048, 128
+    inp = inputs.dense(B, H, H, L, L, d, "bf16", seed=1002, device="cuda", causal=True)
+    o = torch.empty_like(inp.q)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    fl = dense_flops(B, H, L, L, d, True)
+    t = time_steps(lambda: A.attn_fwd(inp.q, inp.k, inp.v, o=o, lse=lse, causal=True), steps,
+                   warm, stream, flush)
+    e = _tensor_entry(fl, statistics.mean(t), pk, A.attn_last_kernel_name())
+    e["roofline"]["traffic"] = traffic_for("prefill_B4H16L2048d128_causal", "prefill_kernel.cuh")
+    return {"dense_causal_prefill_B4_H16_L2048_d128": e}
+
+
 def _extra_gqa(A, inputs, pk, stream, flush, steps, warm):
     inp = inputs.workload(3, device="cuda")
     fl = dense_flops(2, 32, 8192, 8192, 128, True)
@@ -458,7 +505,10 @@ def _extra_gqa(A, inputs, pk, stream, flush, steps, warm):
 def _extra_decode(A, inputs, pk, stream, flush, steps, warm, batch):
     """Paged decode workload; batch < 64 keeps the first `batch` sequence
     lengths of the workload with a pool of just the pages they need (a smaller
-    case for profiling: a few hundred MB on the device)."""
+    case for profiling: a few hundred MB on the device).  `value` is the whole
+    call (split-KV decode kernel + combine kernel); the combine is also timed
+    alone on the same partials, and the decode kernel's own figure is the
+    difference."""
     import torch
     B = min(64, batch)
     if B == 64:
@@ -473,20 +523,33 @@ def _extra_decode(A, inputs, pk, stream, flush, steps, warm, batch):
     lens = inp.seqlens_k[:B].tolist()
     nb = paged_bytes(lens, 8, 128, 1, 32)
     splits = A.attn_paged_auto_splits(B, 8, inp.block_table.shape[1])
-    ws = torch.empty(max(1, splits * B * 32 * 129), dtype=torch.float32, device="cuda")
+    rows = B * 32
+    ws = torch.empty(max(1, splits * rows * 129), dtype=torch.float32, device="cuda")
     o = torch.empty_like(q)
     lse = torch.empty((B, 32, 1), dtype=torch.float32, device="cuda")
     t = time_steps(lambda: A.attn_fwd_paged(q, inp.k_pool, inp.v_pool, bt, sl,
                                             num_splits=splits, o=o, lse=lse, workspace=ws),
                    steps, warm, stream, flush)
+    kernels = A.attn_last_kernel_name()
     ms = statistics.mean(t)
     gbs = nb / (ms * 1e-3) / 1e9
     key = "paged_decode_B64_Hq32_Hkv8_d128_page64" if B == 64 else f"paged_decode_B{B}_Hq32_Hkv8_d128_page64"
-    return {key: {
-        "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "splits": splits,
-        "algorithmic_bytes": nb, "kernel": A.attn_last_kernel_name(),
-        "roofline": {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(gbs / pk["hbm_gbs"], 4)}}}
+    e = {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "splits": splits,
+         "algorithmic_bytes": nb, "kernel": kernels.split("+")[0], "kernels": kernels,
+         "roofline": {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s",
+                      "frac": round(gbs / pk["hbm_gbs"], 4)}}
+    if splits > 1:
+        op = ws[: splits * rows * 128].view(splits, B, 32, 1, 128)
+        lp = ws[splits * rows * 128: splits * rows * 129].view(splits, B, 32, 1)
+        tc = time_steps(lambda: A.attn_splitkv_combine(op, lp, o=o, lse=lse), steps, warm,
+                        stream, flush)
+        ms_c = statistics.mean(tc)
+        ms_d = max(ms - ms_c, 1e-6)
+        e["combine_ms"] = round(ms_c, 4)
+        e["decode_kernel"] = {"ms": round(ms_d, 4), "value": round(nb / (ms_d * 1e-3) / 1e9, 1),
+                              "unit": "GB/s", "frac": round(nb / (ms_d * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                              "note": "whole call minus the combine timed alone"}
+    return {key: e}
 
 
 def _extra_varlen(A, inputs, pk, stream, flush, steps, warm):
@@ -506,13 +569,44 @@ def _extra_varlen(A, inputs, pk, stream, flush, steps, warm):
 
 
 # ---------------------------------------------------------------------------
-def oracle_sample(n_heads):
-    """Inputs of n_heads (batch, head) problems of the headline workload:
-    1 x n_heads x 2048 x 128, causal (same shape as one slice of it)."""
+GQA_L, GQA_D = 8192, 128
+
+
+def oracle_sample(n_heads, rows, seed=1003):
+    """A bounded sample of the GQA causal workload for the fp64 oracle:
+    n_heads query heads (4 per kv head) of one batch, each restricted to the
+    LAST `rows` of its 8192 query rows against all 8192 keys.  With the
+    bottom-right causal mask those rows keep exactly the keys they keep in the
+    full problem, so the work per row is the workload's own."""
     from attention_forward_13_gb300 import inputs
-    inp = inputs.dense(1, n_heads, n_heads, 2048, 2048, 128, "bf16", seed=1002, causal=True)
     import torch
-    return [t.to(torch.float64).numpy() for t in (inp.q, inp.k, inp.v)]
+    hkv = max(1, n_heads // 4)
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((1, n_heads, rows, GQA_D), generator=g).to(torch.bfloat16)
+    kv = inputs.dense(1, hkv, hkv, 1, GQA_L, GQA_D, "bf16", seed=seed)
+    return [t.to(torch.float64).numpy() for t in (q, kv.k, kv.v)]
+
+
+def sample_flops(n_heads, rows):
+    return 4.0 * GQA_D * n_heads * causal_pairs(rows, GQA_L)
+
+
+def size_sample(target_seconds, cores):
+    """(heads, rows) of a sample the oracle finishes in about target_seconds
+    on `cores` threads, from a timed single-head probe of 32 rows."""
+    import oracle
+    q, k, v = oracle_sample(4, 32)
+    t0 = time.perf_counter()  # one (batch, head) problem: one thread does it all
+    oracle.attn_dense(q[:, :1], k[:, :1], v[:, :1], 1 / math.sqrt(GQA_D), True)
+    per_row = (time.perf_counter() - t0) / 32
+    heads = 4 * max(1, (cores + 3) // 4)
+    rows = int(target_seconds * cores / (heads * max(per_row, 1e-6)))
+    return heads, max(16, min(GQA_L, rows))
+
+
+def _oracle_threads(cores):
+    """The oracle's OpenMP thread count (read once, when its library loads)."""
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
 
 
 def cpu_baseline(target_seconds=15.0):
@@ -520,52 +614,53 @@ def cpu_baseline(target_seconds=15.0):
     workload and report the same metric (TFLOP/s on unmasked pairs)."""
     import oracle
     cores = os.cpu_count() or 1
-    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
-    q, k, v = oracle_sample(1)
+    _oracle_threads(cores)
+    heads, rows = size_sample(target_seconds, cores)
+    q, k, v = oracle_sample(heads, rows)
     t0 = time.perf_counter()
-    oracle.attn_dense(q, k, v, 1 / math.sqrt(128), True)
-    one = time.perf_counter() - t0  # wall of one head (single thread)
-    n = max(1, min(64, int(target_seconds * cores / max(one, 1e-3))))
-    q, k, v = oracle_sample(n)
-    t0 = time.perf_counter()
-    oracle.attn_dense(q, k, v, 1 / math.sqrt(128), True)
+    oracle.attn_dense(q, k, v, 1 / math.sqrt(GQA_D), True)
     sec = time.perf_counter() - t0
-    fl = dense_flops(1, n, 2048, 2048, 128, True)
+    fl = sample_flops(heads, rows)
     return {"value": round(fl / sec / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{n} of the 64 (batch, head) problems of the headline workload "
-                      f"(2048x2048 causal, d=128), fp64, {sec:.1f} s wall"}
+            "sample": f"{heads} query heads ({heads // 4} kv heads) of the GQA causal "
+                      f"workload, the last {rows} of 8192 query rows each against all 8192 "
+                      f"keys (d=128), fp64, {sec:.1f} s wall"}
 
 
 def run_reference(args, rank, world):
-    """The oracle timed as the reference arm (rank 0 only)."""
+    """The oracle timed as the reference arm (rank 0 only): W warm-up steps on
+    a tiny sample, then K steps, each the same bounded sample of the headline
+    workload (about 5 s of CPU work)."""
     if rank != 0:
         return None
     import oracle
     cores = os.cpu_count() or 1
-    n = max(1, min(16, cores))
-    q, k, v = oracle_sample(n)
-    fl = dense_flops(1, n, 2048, 2048, 128, True)
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        oracle.attn_dense(q[:, :1], k[:, :1], v[:, :1], 1 / math.sqrt(128), True)
+    _oracle_threads(cores)
+    heads, rows = size_sample(5.0, cores)
+    q, k, v = oracle_sample(heads, rows)
+    fl = sample_flops(heads, rows)
+    for _ in range(args.warmup):
+        oracle.attn_dense(q[:, :1, :16], k[:, :1], v[:, :1], 1 / math.sqrt(GQA_D), True)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.attn_dense(q, k, v, 1 / math.sqrt(128), True)
+        oracle.attn_dense(q, k, v, 1 / math.sqrt(GQA_D), True)
         times.append(time.perf_counter() - t0)
     sec = statistics.mean(times)
     val = fl / sec / 1e12
+    sample = (f"{heads} query heads ({heads // 4} kv heads), the last {rows} of 8192 query "
+              f"rows each against all 8192 keys, per step; fp64 oracle")
     return {
         "impl": "reference",
         "metric": "attn fwd TFLOPS (causal prefill, unmasked pairs) & % of GB300 bf16 tensor peak",
         "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "dense causal prefill B4 H16 L2048 d128 bf16 (bottom-right causal)",
-                   "sample": f"{n} (batch, head) problems per step"},
+        "config": {"workload": "GQA causal prefill B2 Hq32 Hkv8 L8192 d128 bf16 (bottom-right causal)",
+                   "sample": sample},
         "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": cores,
-                         "kind": "oracle",
-                         "sample": f"{n} of 64 (batch, head) problems, fp64 oracle"},
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -581,7 +676,11 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["gqa", "decode", "varlen", "masks", "chunked", "fp8"],
+    ap.add_argument("--passes", type=int, default=0,
+                    help="passes per timed step (0: enough for --min-seconds)")
+    ap.add_argument("--min-seconds", type=float, default=3.0)
+    ap.add_argument("--only", choices=["gqa", "dense", "decode", "varlen", "masks", "chunked",
+                                       "fp8"],
                     default=None,
                     help="run one secondary workload alone (profiling) and print its line")
     ap.add_argument("--decode-batch", type=int, default=64)

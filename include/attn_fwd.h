@@ -192,9 +192,11 @@ attn_status attn_fwd_paged(const void* q, const void* k_pool, const void* v_pool
  *   lse_partial: the split scratch comes from a fixed array of
  *   ATTN_NOALLOC_SCRATCH_BYTES inside this library, reserved on each GPU
  *   that loads the library and held until the process exits.
- *   An explicit num_splits whose scratch (attn_paged_workspace_bytes) would
- *   exceed that size is rejected with ATTN_ERR_INVALID; num_splits = 0 picks
- *   the automatic count, lowered until it fits.  The call allocates and
+ *   For decode (Lq * (Hq / Hkv) <= 16) an explicit num_splits whose scratch
+ *   (attn_paged_workspace_bytes) would exceed that size is rejected with
+ *   ATTN_ERR_INVALID, and num_splits = 0 picks the automatic count, lowered
+ *   until it fits.  Longer chunks run the prefill kernel, which uses no
+ *   scratch: there num_splits is ignored, as in attn_fwd_paged.  The call allocates and
  *   frees no device memory.  The first call on each device looks up the
  *   array's address with that device current; make it before any stream
  *   capture.  All calls on a device share the array: calls whose kernels
@@ -262,7 +264,9 @@ attn_status attn_dense_schedule(int B, int Hq, int Lq, int Lk, const attn_opts* 
 /* Human-readable name of a status. */
 const char* attn_status_string(attn_status status);
 
-/* Trait string of the last kernel this thread launched (empty if none). */
+/* Trait string of the kernel the last call on this thread launched (empty if
+ * none); for a split-KV attn_fwd_paged call, the decode kernel's and the
+ * combine kernel's joined by '+'. */
 const char* attn_last_kernel_name(void);
 
 /* Reads and clears the current device's error word.  Returns ATTN_OK if no

@@ -203,4 +203,4 @@ def mutant_id(mutant: int) -> int:
     return _lib(mutant).oracle_mutant_id()
 
 
-MUTANTS = tuple(range(1, 12))
+MUTANTS = tuple(range(1, 14))

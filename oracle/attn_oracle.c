@@ -215,8 +215,10 @@ int oracle_attn_dense(const double* q, const double* k, const double* v,
                         sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
                         o + (((long)b * Hq + h) * Lq + i) * d,
                         lse + ((long)b * Hq + h) * Lq + i);
-            if (o_scale != 1.0)
+            if (o_scale != 1.0) {
                 for (int t = 0; t < d; ++t) o[(((long)b * Hq + h) * Lq + i) * d + t] *= o_scale;
+                if (MUTANT(12)) lse[((long)b * Hq + h) * Lq + i] *= o_scale; /* scale on LSE too */
+            }
             if (s_out) memcpy(s_out + (((long)b * Hq + h) * Lq + i) * Lk, s_row, sizeof(double) * Lk);
             if (p_out) memcpy(p_out + (((long)b * Hq + h) * Lq + i) * Lk, p_row, sizeof(double) * Lk);
         }
@@ -255,7 +257,7 @@ int oracle_attn_varlen(const double* q, const double* k, const double* v,
                         alibi ? alibi[(long)b * Hq + h] : 0.0,
                         sink != NULL, sink ? sink[h] : 0.0, s_row, p_row, keep,
                         o + (row * Hq + h) * d, lse + (long)h * total_q + row);
-            if (o_scale != 1.0)
+            if (o_scale != 1.0 && !MUTANT(13))                   /* MUTANT 13: scale dropped */
                 for (int t = 0; t < d; ++t) o[(row * Hq + h) * d + t] *= o_scale;
         }
         free(s_row); free(p_row); free(keep);

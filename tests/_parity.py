@@ -1,11 +1,15 @@
 """Helpers for the GPU-vs-oracle parity tests.
 
-Tolerances (fp16/bf16 outputs).  The oracle's O is rounded once to the output
-type (round to nearest even), as the oracle definition states; then per
-element |O_gpu - O_ref| <= max(2e-2, one ulp of the output type at |O_ref|)
-and the mean of |O_gpu - O_ref| <= 2e-3.  The ulp term only matters where
-|O| >= 4 in bf16 (|O| >= 32 in fp16): there one ulp exceeds 2e-2, so two
-correctly rounded results of fp32 values a hair apart can differ by it.
+Tolerances (fp16/bf16 outputs).  The GPU's O is compared with the oracle's
+UNROUNDED fp64 O.  Per element
+    |O_gpu - O_exact| <= 2e-2 + 1/2 ulp(O_exact)
+where the half ulp (of the output type, at |O_exact|) is the rounding every
+correct fp16/bf16 output carries and 2e-2 is the budget for the kernel's own
+arithmetic.  The half ulp is 2^-9 |O| or less in bf16 (2^-12 |O| in fp16):
+below 2e-2 while |O| < 8 in bf16, the larger term from |O| >= 8 on.  The
+mean of |O_gpu - O_exact| (rounding included) must stay <= 2e-3.  check()
+also counts the elements whose error exceeds 2e-2 (those that needed the
+half-ulp term) and returns them in its statistics.
 LSE: abs <= 1e-3; an LSE of -inf must match exactly.
 """
 import math
@@ -40,19 +44,25 @@ def ulp(x: np.ndarray, dtype) -> np.ndarray:
     return np.exp2(np.floor(np.log2(ax)) - m)
 
 
-def check(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+def check(o_gpu, lse_gpu, o_ref, lse_ref, what="", stats=None):
+    """Compare GPU O/LSE with the unrounded fp64 oracle; returns the max O error.
+    If ``stats`` is a dict it receives the max error, the mean error, the count
+    of elements above 2e-2 and the largest |O_exact| among them, and the max
+    LSE error."""
     dtype = o_gpu.dtype if isinstance(o_gpu, torch.Tensor) else torch.float32
     o = f64(o_gpu) if isinstance(o_gpu, torch.Tensor) else o_gpu
     assert o.shape == o_ref.shape, (what, o.shape, o_ref.shape)
     assert np.all(np.isfinite(o)), f"{what}: non-finite O"
-    ref = round_to(o_ref, dtype)
-    err = np.abs(o - ref)
-    bound = np.maximum(O_MAX, ulp(ref, dtype))
+    err = np.abs(o - o_ref)
+    bound = O_MAX + 0.5 * ulp(o_ref, dtype)
     if err.size:
         i = np.unravel_index(np.argmax(err - bound), err.shape)
-        assert np.all(err <= bound), (f"{what}: O err {err[i]} at |O|={abs(ref[i])} "
+        assert np.all(err <= bound), (f"{what}: O err {err[i]} at |O|={abs(o_ref[i])} "
                                       f"(bound {bound[i]}), max err {err.max()}")
-    assert (err.mean() if err.size else 0.0) <= O_MEAN, f"{what}: O mean err {err.mean()}"
+    mean = float(err.mean()) if err.size else 0.0
+    assert mean <= O_MEAN, f"{what}: O mean err {mean}"
+    over = err > O_MAX
+    lse_err = 0.0
     if lse_gpu is not None:
         lg = f64(lse_gpu) if isinstance(lse_gpu, torch.Tensor) else lse_gpu
         assert lg.shape == lse_ref.shape, (what, lg.shape, lse_ref.shape)
@@ -61,8 +71,37 @@ def check(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
         fin = ~inf_ref
         if fin.any():
             e = np.abs(lg[fin] - lse_ref[fin])
-            assert e.max() <= LSE_TOL, f"{what}: LSE max err {e.max()}"
+            lse_err = float(e.max())
+            assert lse_err <= LSE_TOL, f"{what}: LSE max err {lse_err}"
+    if stats is not None:
+        stats.update(max_err=float(err.max(initial=0.0)), mean_err=mean,
+                     n=int(err.size), n_over_2e2=int(over.sum()),
+                     max_abs_o_over=float(np.abs(o_ref[over]).max(initial=0.0)),
+                     lse_max_err=lse_err)
     return float(err.max(initial=0.0))
+
+
+def merge_stats(total, part):
+    """Accumulate check() statistics over pieces of one output."""
+    if not total:
+        total.update(part)
+        total["_sum"] = part["mean_err"] * part["n"]
+        return total
+    total["_sum"] = total.get("_sum", 0.0) + part["mean_err"] * part["n"]
+    total["n"] += part["n"]
+    total["mean_err"] = total["_sum"] / max(total["n"], 1)
+    for k in ("max_err", "max_abs_o_over", "lse_max_err"):
+        total[k] = max(total[k], part[k])
+    total["n_over_2e2"] += part["n_over_2e2"]
+    return total
+
+
+def report(what, stats):
+    """One line per full-size comparison (shown with pytest -s or -rP)."""
+    print(f"PARITY {what}: {stats['n']} O elements, max |dO| {stats['max_err']:.4g}, "
+          f"mean |dO| {stats['mean_err']:.3g}, above 2e-2: {stats['n_over_2e2']} "
+          f"(largest |O| there {stats['max_abs_o_over']:.3g}), max |dLSE| "
+          f"{stats['lse_max_err']:.3g}")
 
 
 # ---------------------------------------------------------------------------
@@ -139,19 +178,25 @@ def dense_case(inp, scale=None):
     return check(o, lse, ro, rl, "dense")
 
 
-def dense_rows_reference(q, k, v, b, h, rows, g, causal, scale, softcap=0.0, sink=None):
-    """Oracle on query rows [r0, r1) of head (b, h) only.  For bottom-right
-    causal masking the key range is cut to what row r1-1 can see, which keeps
-    every row's mask identical to the full problem."""
-    r0, r1 = rows
-    Lq, Lk = q.shape[2], k.shape[2]
-    hk = h // g
-    kend = min(Lk, r1 + (Lk - Lq)) if causal else Lk
-    kend = max(kend, 0)
-    qs = f64(q[b:b + 1, h:h + 1, r0:r1])
-    ks = f64(k[b:b + 1, hk:hk + 1, :kend])
-    vs = f64(v[b:b + 1, hk:hk + 1, :kend])
-    # With kend = r1 + Lk - Lq, row i' of the cut problem keeps
-    # j <= i' + kend - (r1 - r0) = (r0 + i') + (Lk - Lq): the full problem's mask.
-    sk = None if sink is None else f64(sink[h:h + 1])
-    return oracle.attn_dense(qs, ks, vs, scale, causal, softcap, sk)
+def compact_paged(inp, bsel):
+    """The chosen sequences of a paged problem with only their own pages, in
+    fp64, and a renumbered block table (bounds the oracle's host memory on a
+    large pool)."""
+    page = inp.page_size
+    bt = inp.block_table
+    lens = inp.seqlens_k
+    pages, rows = [], []
+    for b in bsel:
+        n = (int(lens[b]) + page - 1) // page
+        ids = bt[b, :n].tolist()
+        rows.append(list(range(len(pages), len(pages) + n)))
+        pages.extend(ids)
+    idx = torch.tensor(pages, dtype=torch.long, device=inp.k_pool.device)
+    kp = f64(inp.k_pool.index_select(0, idx))
+    vp = f64(inp.v_pool.index_select(0, idx))
+    maxn = max(max(len(r) for r in rows), 1)
+    nbt = np.zeros((len(bsel), maxn), dtype=np.int32)
+    for i, r in enumerate(rows):
+        nbt[i, :len(r)] = r
+    return kp, vp, nbt, lens[list(bsel)].numpy()
+

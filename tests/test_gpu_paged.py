@@ -1,6 +1,7 @@
 """GPU parity of the paged-KV split-KV kernel and the split combine against the
 fp64 oracle, including empty sequences, partial last pages, empty splits,
-causal chunks and the full-size paged decode workload (sampled sequences)."""
+causal chunks; the full-size decode workload is compared whole in
+test_gpu_full_size.py."""
 import math
 
 import numpy as np
@@ -96,45 +97,6 @@ def test_combine_parity():
         ro, rl = oracle.combine(f64(op).reshape(S, rows, d), f64(lp).reshape(S, rows), sink_rows)
         check(o, lse, ro.reshape(B, Hq, Lq, d).transpose(0, 2, 1, 3), rl.reshape(B, Hq, Lq),
               f"combine S={S}")
-    no_device_error()
-
-
-def _compact(inp, bsel):
-    """The chosen sequences with only their own pages (the oracle then gathers
-    through a renumbered block table)."""
-    page = inp.page_size
-    bt = inp.block_table
-    lens = inp.seqlens_k
-    pages, rows = [], []
-    for b in bsel:
-        n = (int(lens[b]) + page - 1) // page
-        ids = bt[b, :n].tolist()
-        rows.append(list(range(len(pages), len(pages) + n)))
-        pages.extend(ids)
-    idx = torch.tensor(pages, dtype=torch.long, device=inp.k_pool.device)
-    kp = f64(inp.k_pool.index_select(0, idx))
-    vp = f64(inp.v_pool.index_select(0, idx))
-    maxn = max(len(r) for r in rows)
-    nbt = np.zeros((len(bsel), maxn), dtype=np.int32)
-    for i, r in enumerate(rows):
-        nbt[i, :len(r)] = r
-    return kp, vp, nbt, lens[list(bsel)].numpy()
-
-
-def test_workload4_full_size_sampled():
-    """Paged decode B64 Hq32 Hkv8 d128 page 64 over a 10240-page pool at full
-    size (auto splits + combine); five sequences checked against the oracle."""
-    inp = inputs.workload(4, device="cuda")
-    o, lse = A.attn_fwd_paged(inp.q, inp.k_pool, inp.v_pool, inp.block_table.cuda(),
-                              inp.seqlens_k.cuda())
-    torch.cuda.synchronize()
-    lens = inp.seqlens_k.tolist()
-    order = np.argsort(lens)
-    bsel = [int(order[0]), int(order[1]), int(order[32]), int(order[-2]), int(order[-1])]
-    kp, vp, nbt, sl = _compact(inp, bsel)
-    qsel = f64(inp.q[bsel])
-    ro, rl = oracle.attn_paged(qsel, kp, vp, nbt, sl, 1 / math.sqrt(128))
-    check(o[bsel], lse[bsel], ro, rl, "workload 4")
     no_device_error()
 
 

@@ -1,16 +1,15 @@
 """GPU parity of the dense and varlen (group-mode) prefill kernel against the
-fp64 oracle, element by element, on seeded inputs; plus sampled rows of the
-full-size dense workloads."""
+fp64 oracle, element by element, on seeded inputs (the full-size workloads
+are compared whole in test_gpu_full_size.py)."""
 import math
 
-import numpy as np
 import pytest
 import torch
 
 import oracle
 import attention_forward_13_gb300 as A
 from attention_forward_13_gb300 import inputs
-from tests._parity import check, cuda, dense_case, dense_rows_reference, f64, no_device_error
+from tests._parity import check, cuda, dense_case, f64, no_device_error
 
 pytestmark = pytest.mark.gpu
 
@@ -108,57 +107,4 @@ def test_varlen_parity(case):
                                 inp.cu_seqlens_k.numpy(), 1 / math.sqrt(d), causal, cap,
                                 None if inp.sink is None else f64(inp.sink))
     check(o, lse, ro, rl, "varlen")
-    no_device_error()
-
-
-def _sampled_dense(inp, picks, g):
-    d = inp.q.shape[-1]
-    sc = 1 / math.sqrt(d)
-    o, lse = A.attn_fwd(inp.q, inp.k, inp.v, causal=inp.causal)
-    torch.cuda.synchronize()
-    worst = 0.0
-    for b, h, r0, r1 in picks:
-        ro, rl = dense_rows_reference(inp.q, inp.k, inp.v, b, h, (r0, r1), g, inp.causal, sc)
-        worst = max(worst, check(o[b:b + 1, h:h + 1, r0:r1], lse[b:b + 1, h:h + 1, r0:r1], ro,
-                                 rl, f"rows b{b} h{h} {r0}:{r1}"))
-    no_device_error()
-    return worst
-
-
-def test_workload2_full_size_sampled():
-    """Dense causal prefill B4 H16 L2048 d128 at full size, sampled rows."""
-    inp = inputs.workload(2, device="cuda")
-    picks = [(0, 0, 0, 64), (1, 7, 1000, 1064), (3, 15, 1984, 2048), (2, 3, 255, 257)]
-    _sampled_dense(inp, picks, 1)
-
-
-def test_workload3_full_size_sampled():
-    """GQA causal prefill B2 Hq32 Hkv8 L8192 d128 at full size, sampled rows."""
-    inp = inputs.workload(3, device="cuda")
-    picks = [(0, 0, 0, 32), (0, 5, 4095, 4127), (1, 31, 8160, 8192), (1, 12, 8000, 8032)]
-    _sampled_dense(inp, picks, 4)
-
-
-def test_workload5_full_size_sampled():
-    """Varlen causal prefill with softcap 30 and sinks: 16 sequences in
-    [128, 4096], sampled sequences compared in full."""
-    inp = inputs.workload(5, device="cuda")
-    cu = inp.cu_seqlens_q
-    o, lse = A.attn_fwd_varlen(inp.q, inp.k, inp.v, cu.cuda(), inp.cu_seqlens_k.cuda(),
-                               inp.max_seqlen_q, causal=True, softcap=30.0, sink=inp.sink)
-    torch.cuda.synchronize()
-    lens = (cu[1:] - cu[:-1]).tolist()
-    order = np.argsort(lens)
-    for bsel in (int(order[0]), int(order[len(order) // 2]), int(order[-1])):
-        s0, s1 = int(cu[bsel]), int(cu[bsel + 1])
-        # the sequence alone, rows [max(0, L-192), L): the last rows see every key
-        r0 = max(0, (s1 - s0) - 192)
-        q = f64(inp.q[s0 + r0:s1])
-        k = f64(inp.k[s0:s1])
-        v = f64(inp.v[s0:s1])
-        cq = np.array([0, s1 - s0 - r0], dtype=np.int32)
-        # the cut keeps bottom-right alignment: Lk - Lq' = r0
-        ro, rl = oracle.attn_varlen(q, k, v, cq, np.array([0, s1 - s0], dtype=np.int32),
-                                    1 / math.sqrt(64), True, 30.0, f64(inp.sink))
-        check(o[s0 + r0:s1], lse[:, s0 + r0:s1], ro, rl, f"seq {bsel}")
     no_device_error()

@@ -4,9 +4,11 @@ fix, never against the oracle itself or the CUDA path.
 Each ``pin_*`` function raises AssertionError on a mismatch and takes the
 oracle variant to check (0 = the real oracle, n > 0 = a build with planted
 mistake n).  ``test_mutants_are_caught`` proves the pins have teeth: every
-planted mistake (wrong index, dropped scale, dropped cap, top-left causal,
-dropped sink, dropped max term, transposed V, interleaved GQA grouping) fails
-at least one pin.
+planted mistake (see oracle.MUTANTS and the MUTANT() sites of attn_oracle.c:
+wrong index, dropped scale, dropped cap, top-left causal, dropped sink,
+dropped max term, transposed V, interleaved GQA grouping, a left-window bound
+off by one, a flipped ALiBi sign, a shifted bias row, the output scale applied
+to LSE, the output scale dropped in group mode) fails at least one pin.
 """
 import json
 import math
@@ -55,7 +57,7 @@ def pin_golden(mutant=0):
     for c in cases["dense"]:
         q, k, v = (np.array(c[x], dtype=np.float64) for x in ("q", "k", "v"))
         o, lse = oracle.attn_dense(q, k, v, c["scale"], c["causal"], c["softcap"],
-                                   c["sink"], mutant=mutant)
+                                   c["sink"], mutant=mutant, o_scale=c.get("o_scale", 1.0))
         _close(o, _evtree(c["expect_o"]), 1e-13, c["name"] + " O")
         _close(lse, _evtree(c["expect_lse"]), 1e-13, c["name"] + " LSE")
     for c in cases["combine"]:
@@ -424,10 +426,38 @@ def pin_bias_alibi_top_left(mutant=0):
     _close(o7[:, :, 0], v[:, :, 0], 1e-14, "top-left causal row 0 is V[0]")
 
 
+def pin_output_scale(mutant=0):
+    """FP8 static quantisation's output scale (Composable Kernel
+    FmhaFwdFp8StaticQuantKargs: O's accumulator times scale_o, P times scale_p;
+    reading: O = scale_o * scale_p * softmax(S) V and LSE is not scaled).  For
+    dense and group mode: O(s) equals s * O(1) exactly (one fp64 multiply of
+    the same value on both sides), LSE(s) equals LSE(1) exactly."""
+    rng = _rng(77)
+    q, k, v = (rng.standard_normal(sh) for sh in ((2, 4, 5, 8), (2, 2, 7, 8), (2, 2, 7, 8)))
+    sink = rng.standard_normal(4)
+    for s in (2.0, 0.3):
+        o1, l1 = oracle.attn_dense(q, k, v, 0.4, True, 0.0, sink, mutant=mutant)
+        os_, ls = oracle.attn_dense(q, k, v, 0.4, True, 0.0, sink, mutant=mutant, o_scale=s)
+        _close(os_, s * o1, 0.0, f"dense O(o_scale={s}) = s O(1)")
+        _close(ls, l1, 0.0, f"dense LSE(o_scale={s}) = LSE(1)")
+    lens = [3, 0, 6]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    qv = rng.standard_normal((int(cu[-1]), 4, 8))
+    kv_ = rng.standard_normal((int(cu[-1]), 2, 8))
+    vv = rng.standard_normal((int(cu[-1]), 2, 8))
+    for s in (2.0, 0.3):
+        o1, l1 = oracle.attn_varlen(qv, kv_, vv, cu, cu, 0.4, True, 0.0, sink, mutant=mutant)
+        os_, ls = oracle.attn_varlen(qv, kv_, vv, cu, cu, 0.4, True, 0.0, sink, mutant=mutant,
+                                     o_scale=s)
+        _close(os_, s * o1, 0.0, f"varlen O(o_scale={s}) = s O(1)")
+        _close(ls, l1, 0.0, f"varlen LSE(o_scale={s}) = LSE(1)")
+
+
 PINS = [pin_golden, pin_rows_sum_to_one, pin_identical_keys, pin_one_hot, pin_lse_fsum,
         pin_causal_row0, pin_empty_rows, pin_brute_force, pin_softcap_limits, pin_sink_limits,
         pin_gqa_equals_repeated_mha, pin_paged_equals_contiguous, pin_splits_combine_to_unsplit,
-        pin_varlen_equals_per_sequence, pin_window, pin_bias_alibi_top_left]
+        pin_varlen_equals_per_sequence, pin_window, pin_bias_alibi_top_left,
+        pin_output_scale]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])

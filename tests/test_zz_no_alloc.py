@@ -1,21 +1,27 @@
-"""attn_fwd_paged_noalloc against attn_fwd_paged, through the C ABI.
+"""attn_fwd_paged_noalloc through the C ABI, against the fp64 oracle and
+against attn_fwd_paged with caller-provided scratch.
 
 The no-allocation entry point serves callers that cannot allocate device
 memory at call time (a plugin whose host engine owns every allocation, a
 serving loop that must not call cudaMalloc because it can synchronise the
 device).  It takes its split-KV scratch from a fixed array inside the
-library instead of caller buffers.  Two calls in a row, with different
-shapes and split counts, must each give the result of attn_fwd_paged with
-caller-provided scratch, within the parity tolerance of the other tests; the
-second call checks that what the first left in the shared array does not
-leak into it.  This file is collected last so a run stopping at the first
+library instead of caller buffers.  Calls in a row, with different shapes
+and split counts, must each match the oracle within the parity tolerance of
+the other tests and equal attn_fwd_paged bit for bit at the same split
+count; the later calls check that what an earlier call left in the shared
+array does not leak into them.  Also covered: an automatic split count that
+is lowered to fit the array, and a chunked prefill (more than 16 query rows
+per kv head) with an explicit split count, which needs no scratch and must
+not be rejected.  This file is collected last so a run stopping at the first
 failure has already run every other test.
 """
 import ctypes
+import math
 
 import pytest
 import torch
 
+import oracle
 import attention_forward_13_gb300 as A
 from attention_forward_13_gb300 import _lib, inputs
 from tests._parity import check, f64, no_device_error
@@ -55,14 +61,59 @@ def _with_scratch(inp, splits):
     return o, lse
 
 
-def test_noalloc_matches_scratch_path_two_calls():
+def _oracle(inp):
+    d = inp.q.shape[-1]
+    return oracle.attn_paged(f64(inp.q), f64(inp.k_pool), f64(inp.v_pool),
+                             inp.block_table.numpy(), inp.seqlens_k.numpy(), 1 / math.sqrt(d),
+                             inp.causal, inp.softcap,
+                             None if inp.sink is None else f64(inp.sink))
+
+
+def _case(inp, splits, scratch_splits, what):
+    o, lse = _noalloc_via_abi(inp, splits)
+    ro, rl = _oracle(inp)
+    check(o, lse, ro, rl, f"noalloc {what} vs oracle")
+    o_ref, l_ref = _with_scratch(inp, scratch_splits)
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref), f"noalloc {what} vs scratch path"
+
+
+def test_noalloc_calls_in_a_row():
     first = inputs.paged([700, 64, 1, 2000], 1, 32, 8, 128, 64, 60, seed=314, with_sink=True)
     second = inputs.paged([90, 400, 33], 2, 8, 2, 128, 16, 40, seed=2718, causal=True,
                           softcap=30.0)
-    for inp, splits in ((first, 4), (second, 3)):
-        o_ref, l_ref = _with_scratch(inp, splits)
-        o, lse = _noalloc_via_abi(inp, splits)
-        check(o, lse, f64(o_ref), f64(l_ref), f"noalloc splits={splits}")
+    for inp, splits in ((first, 4), (second, 3), (first, 2)):
+        _case(inp, splits, splits, f"splits={splits}")
+    no_device_error()
+
+
+def test_noalloc_lowers_the_automatic_split_count():
+    """B64 Hq32 Hkv8 Lq4 d128 with a 128-column block table: the automatic
+    count (4) needs more scratch than the array holds, so the call runs with
+    the largest count that fits (3)."""
+    B, Lq, Hq, Hkv, d, page, max_pages = 64, 4, 32, 8, 128, 64, 128
+    auto = A.attn_paged_auto_splits(B, Hkv, max_pages)
+    assert A.attn_paged_workspace_bytes(B, Lq, Hq, d, auto) > _lib.NOALLOC_SCRATCH_BYTES
+    fit = auto
+    while fit > 1 and A.attn_paged_workspace_bytes(B, Lq, Hq, d, fit) > _lib.NOALLOC_SCRATCH_BYTES:
+        fit -= 1
+    assert 1 < fit < auto
+    lens = inputs.random_lengths(B, 4, 3000, seed=55)
+    npages = sum((L + page - 1) // page for L in lens) + 8
+    inp = inputs.paged(lens, Lq, Hq, Hkv, d, page, npages, max_pages=max_pages, seed=56,
+                       causal=True)
+    _case(inp, 0, fit, f"auto splits lowered {auto}->{fit}")
+    no_device_error()
+
+
+def test_noalloc_chunked_prefill_ignores_num_splits():
+    """Lq * Hq / Hkv > 16 runs the prefill kernel, which uses no scratch; an
+    explicit split count whose nominal scratch would not fit is not rejected."""
+    lens, Lq, Hq, Hkv, d, page = [600, 1100, 300], 256, 16, 4, 128, 32
+    assert A.attn_paged_workspace_bytes(len(lens), Lq, Hq, d, 64) > _lib.NOALLOC_SCRATCH_BYTES
+    npages = sum((L + page - 1) // page for L in lens) + 4
+    inp = inputs.paged(lens, Lq, Hq, Hkv, d, page, npages, seed=57, causal=True,
+                       with_sink=True)
+    _case(inp, 64, 0, "chunked prefill, num_splits=64")
     no_device_error()
 
 
