@@ -22,7 +22,7 @@ from . import _lib
 __all__ = ["attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_splitkv_combine",
            "attn_paged_workspace_bytes", "attn_paged_auto_splits", "attn_device_error",
            "attn_selftest_timeout", "attn_last_kernel_name", "attn_paged_window_pages",
-           "attn_fwd_paged_noalloc", "attn_dense_schedule", "AttnError", "library"]
+           "attn_fwd_paged_noalloc", "attn_dense_schedule", "gqa_pack", "AttnError", "library"]
 
 
 class AttnError(RuntimeError):
@@ -202,15 +202,26 @@ def attn_paged_window_pages(Lq, page_size, max_pages_per_seq, window=None, causa
                                                  ctypes.byref(opts)))
 
 
-def attn_dense_schedule(B, Hq, Lq, Lk, grid, causal=False, window=None, top_left=False):
+def gqa_pack(Hq, Hkv) -> int:
+    """Query heads per tile the library packs for Hq / Hkv (PackGQA): g when
+    g = Hq / Hkv is 2, 4, 8 or 16, else 1."""
+    g = Hq // Hkv if Hkv > 0 and Hq % Hkv == 0 else 1
+    return g if g in (2, 4, 8, 16) else 1
+
+
+def attn_dense_schedule(B, Hq, Lq, Lk, grid, causal=False, window=None, top_left=False, Hkv=None):
     """The static schedule attn_fwd runs on `grid` CTAs for a dense masked
     problem: a list of `grid` lists of work items (CTA by CTA, in run order),
-    or None where the problem keeps the plain snake order."""
+    or None where the problem keeps the plain snake order.  Hkv defaults to
+    Hq (no head packing)."""
+    Hkv = Hq if Hkv is None else Hkv
     opts = _opts(None, causal, 0.0, None, window, top_left)
-    n = B * Hq * ((Lq + 255) // 256) if Lq > 0 else 0
+    pack = gqa_pack(Hq, Hkv)
+    per = 256 // pack
+    n = B * (Hq // pack) * ((Lq + per - 1) // per) if Lq > 0 else 0
     off = (ctypes.c_int32 * (max(grid, 0) + 1))()
     item = (ctypes.c_int32 * max(n, 1))()
-    st = library().attn_dense_schedule(B, Hq, Lq, Lk, ctypes.byref(opts), grid, off, item)
+    st = library().attn_dense_schedule(B, Hq, Hkv, Lq, Lk, ctypes.byref(opts), grid, off, item)
     if st == 2:
         return None
     _check(st, "attn_dense_schedule")

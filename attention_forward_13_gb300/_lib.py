@@ -61,7 +61,7 @@ def _declare(lib):
     lib.attn_paged_window_pages.argtypes = [_I, _I, _I, O]
     lib.attn_paged_window_pages.restype = _I
     IP = ctypes.POINTER(ctypes.c_int32)
-    lib.attn_dense_schedule.argtypes = [_I, _I, _I, _I, O, _I, IP, IP]
+    lib.attn_dense_schedule.argtypes = [_I, _I, _I, _I, _I, O, _I, IP, IP]
     lib.attn_dense_schedule.restype = _I
     lib.attn_status_string.argtypes = [_I]
     lib.attn_status_string.restype = ctypes.c_char_p

@@ -131,8 +131,37 @@ void resolve_window(const attn_opts* opts, int* wl, int* wr) {
   if (opts->causal) *wr = 0;  // any window_right >= 0 is looser than causal
 }
 
-// 256-row query blocks of L rows (no int overflow for any L >= 0).
-int m_blocks(int L) { return static_cast<int>((static_cast<int64_t>(L) + 255) / 256); }
+// PackGQA (FlashAttention-3 epilogue, PackGQA row <-> (head, query) mapping):
+// the g = Hq / Hkv query heads of a kv head share each 128-row tile, 128 / g
+// queries of each, when g is a power of two from 2 to 16 (the tile then
+// holds whole queries of every head of the group, and one TMA box loads it).
+#ifndef ATTN_PACK_GQA
+#define ATTN_PACK_GQA 1
+#endif
+int pack_of(int Hq, int Hkv) {
+  const int g = Hq / Hkv;
+  if (!ATTN_PACK_GQA || Hq % Hkv != 0) return 1;
+  return (g == 2 || g == 4 || g == 8 || g == 16) ? g : 1;
+}
+int log2_int(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+// Query blocks (two 128-row tiles of 128 / pack queries each) of L queries
+// (no int overflow for any L >= 0).
+int m_blocks(int L, int pack = 1) {
+  const int64_t per = 256 / pack;
+  return static_cast<int>((static_cast<int64_t>(L) + per - 1) / per);
+}
+
+// Packing fields of the launch parameters.
+void set_pack(PrefillParams& p, int Hq, int Hkv) {
+  p.pack = pack_of(Hq, Hkv);
+  p.qpt_log2 = log2_int(128 / p.pack);
+  p.units = Hq / p.pack;
+}
 
 void fill_common(PrefillParams& p, const attn_opts* opts, int d) {
   const float scale = resolve_scale(opts, d);
@@ -270,14 +299,15 @@ struct Schedule {
 // K/V steps of query block mb (two 128-row tiles) in a dense problem: the
 // union of both tiles' key ranges, as the kernel's item decode computes it.
 int dense_block_steps(const PrefillParams& p, int mb) {
-  constexpr int BM = 128, BN = 128;
-  const int m0 = mb * 2 * BM;
+  constexpr int BN = 128;
+  const int qpt = 1 << p.qpt_log2;  // queries per tile
+  const int m0 = mb * 2 * qpt;
   const int diag = p.top_left ? 0 : p.Lk - p.Lq;
   int jb = INT_MAX, je = 0;
   for (int t = 0; t < 2; ++t) {
-    const int mt = m0 + t * BM;
+    const int mt = m0 + t * qpt;
     if (mt >= p.Lq) continue;
-    const int last = std::min(mt + BM - 1, p.Lq - 1);
+    const int last = std::min(mt + qpt - 1, p.Lq - 1);
     int kend = p.Lk, kbeg = 0;
     if (p.win_right >= 0) kend = std::min(p.Lk, last + diag + p.win_right + 1);
     if (p.win_left >= 0) kbeg = std::max(0, mt + diag - p.win_left);
@@ -291,14 +321,15 @@ int dense_block_steps(const PrefillParams& p, int mb) {
 
 std::shared_ptr<const Schedule> dense_schedule(const PrefillParams& p, int grid) {
   static std::mutex mu;
-  static std::map<std::array<int, 8>, std::shared_ptr<const Schedule>> cache;
-  const std::array<int, 8> key = {p.B, p.Hq, p.Lq, p.Lk, p.win_left, p.win_right, p.top_left, grid};
+  static std::map<std::array<int, 9>, std::shared_ptr<const Schedule>> cache;
+  const std::array<int, 9> key = {p.B, p.units, p.Lq, p.Lk, p.win_left, p.win_right, p.top_left,
+                                  p.qpt_log2, grid};
   {
     std::lock_guard<std::mutex> lock(mu);
     const auto f = cache.find(key);
     if (f != cache.end()) return f->second;
   }
-  const int n = p.num_items, nbh = p.B * p.Hq;
+  const int n = p.num_items, nbh = p.B * p.units;
   // Cost in tenths of a K/V step: the steps plus a fixed per-item share of
   // four steps (the Q load and first S before any PV, the last PV and the
   // epilogue); of the shares 0, 1.6, 4 and 8 steps, 4 gave the shortest
@@ -460,7 +491,9 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     const attn_status so_ = check_opts(opts, Hq, true);
     if (so_ != ATTN_OK) return so_;
   }
-  if (static_cast<int64_t>(B) * Hq * m_blocks(Lq) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * (Hq / pack_of(Hq, Hkv)) * m_blocks(Lq, pack_of(Hq, Hkv)) >
+      0x7fffffffLL)
+    return ATTN_ERR_UNSUPPORTED;
 
   PrefillParams p;
   memset(&p, 0, sizeof(p));
@@ -468,11 +501,13 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   int num_sms = 0;
   if (device_state(&err, &num_sms) != ATTN_OK) return ATTN_ERR_CUDA;
   const int dt = dtype == ATTN_E4M3 ? kDtE4M3 : dtype == ATTN_BF16 ? kDtBF16 : kDtF16;
+  set_pack(p, Hq, Hkv);
   const uint32_t box[4] = {(uint32_t)(128 / eb), 128, 1, 1};
   {
+    const uint32_t qbox[4] = {(uint32_t)(128 / eb), (uint32_t)(128 / p.pack), (uint32_t)p.pack, 1};
     const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lq, (uint64_t)Hq, (uint64_t)B};
     const uint64_t st[3] = {(uint64_t)sq.row * eb, (uint64_t)sq.head * eb, (uint64_t)sq.batch * eb};
-    if (!make_map(&p.tm_q, q, dtype, 4, dims, st, box)) return ATTN_ERR_INVALID;
+    if (!make_map(&p.tm_q, q, dtype, 4, dims, st, qbox)) return ATTN_ERR_INVALID;
   }
   if (Lk > 0) {  // Lk = 0: no key tile is ever loaded, the maps stay unused
     {
@@ -501,7 +536,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.Hkv = Hkv;
   p.Lq = Lq;
   p.Lk = Lk;
-  p.num_m_blocks = m_blocks(Lq);
+  p.num_m_blocks = m_blocks(Lq, p.pack);
   p.err = err;
   fill_common(p, opts, d);
   if (opts != nullptr && opts->bias != nullptr) {
@@ -511,7 +546,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     p.bias_batch = opts->bias_strides.batch;
   }
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
-  p.num_items = p.num_m_blocks * B * Hq;
+  p.num_items = p.num_m_blocks * B * p.units;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
   attach_schedule(p, grid);
   return finish_launch(launch_prefill(p, grid, d, dt, masked, score_xf(p),
@@ -543,7 +578,8 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
     return ATTN_ERR_INVALID;
   for (const attn_strides* s : {&sq, &sk, &sv, &so})
     if (!stride_ok(s->row, eb) || !stride_ok(s->head, eb)) return ATTN_ERR_INVALID;
-  if (static_cast<int64_t>(B) * Hq * m_blocks(max_seqlen_q) > 0x7fffffffLL)
+  if (static_cast<int64_t>(B) * (Hq / pack_of(Hq, Hkv)) *
+          m_blocks(max_seqlen_q, pack_of(Hq, Hkv)) > 0x7fffffffLL)
     return ATTN_ERR_UNSUPPORTED;
   {
     const attn_status so_ = check_opts(opts, Hq, false);
@@ -556,12 +592,14 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   int num_sms = 0;
   if (device_state(&err, &num_sms) != ATTN_OK) return ATTN_ERR_CUDA;
   const int dt = dtype == ATTN_E4M3 ? kDtE4M3 : dtype == ATTN_BF16 ? kDtBF16 : kDtF16;
+  set_pack(p, Hq, Hkv);
   const uint32_t box[4] = {(uint32_t)(128 / eb), 128, 1, 1};
   {
+    const uint32_t qbox[4] = {(uint32_t)(128 / eb), (uint32_t)(128 / p.pack), (uint32_t)p.pack, 1};
     const uint64_t dims[4] = {(uint64_t)d, (uint64_t)total_q, (uint64_t)Hq, 1};
     const uint64_t st[3] = {(uint64_t)sq.row * eb, (uint64_t)sq.head * eb,
                             (uint64_t)sq.row * eb * (uint64_t)total_q};
-    if (!make_map(&p.tm_q, q, dtype, 4, dims, st, box)) return ATTN_ERR_INVALID;
+    if (!make_map(&p.tm_q, q, dtype, 4, dims, st, qbox)) return ATTN_ERR_INVALID;
   }
   if (total_k > 0) {  // no keys at all: the maps stay unused
     const int tk = total_k;
@@ -594,11 +632,11 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   p.Hkv = Hkv;
   p.Lq = 0;
   p.Lk = 0;
-  p.num_m_blocks = m_blocks(max_seqlen_q);
+  p.num_m_blocks = m_blocks(max_seqlen_q, p.pack);
   p.err = err;
   fill_common(p, opts, d);
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
-  p.num_items = p.num_m_blocks * B * Hq;
+  p.num_items = p.num_m_blocks * B * p.units;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;  // persistent: one CTA per SM
   return finish_launch(launch_prefill(p, grid, d, dt, masked, score_xf(p),
                                       static_cast<cudaStream_t>(stream), g_last_name,
@@ -617,14 +655,17 @@ attn_status paged_prefill(const void* q, const void* k_pool, const void* v_pool,
                           float* lse, int B, int Lq, int Hq, int Hkv, int d, bool bf16,
                           int page_size, int num_pages, int max_pages, const attn_opts* opts,
                           cudaStream_t stream) {
-  if (static_cast<int64_t>(B) * Hq * m_blocks(Lq) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * (Hq / pack_of(Hq, Hkv)) * m_blocks(Lq, pack_of(Hq, Hkv)) >
+      0x7fffffffLL)
+    return ATTN_ERR_UNSUPPORTED;
   PrefillParams p;
   memset(&p, 0, sizeof(p));
   unsigned int* err = nullptr;
   int num_sms = 0;
   if (device_state(&err, &num_sms) != ATTN_OK) return ATTN_ERR_CUDA;
+  set_pack(p, Hq, Hkv);
   {
-    const uint32_t box[4] = {64, 128, 1, 1};
+    const uint32_t box[4] = {64, (uint32_t)(128 / p.pack), (uint32_t)p.pack, 1};
     const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lq, (uint64_t)Hq, (uint64_t)B};
     const uint64_t st[3] = {(uint64_t)Hq * d * 2, (uint64_t)d * 2, (uint64_t)Lq * Hq * d * 2};
     if (!make_map(&p.tm_q, q, bf16 ? ATTN_BF16 : ATTN_F16, 4, dims, st, box)) return ATTN_ERR_INVALID;
@@ -648,7 +689,7 @@ attn_status paged_prefill(const void* q, const void* k_pool, const void* v_pool,
   p.Hkv = Hkv;
   p.Lq = Lq;
   p.Lk = max_pages * page_size;
-  p.num_m_blocks = m_blocks(Lq);
+  p.num_m_blocks = m_blocks(Lq, p.pack);
   p.err = err;
   fill_common(p, opts, d);
   p.block_table = block_table;
@@ -657,7 +698,7 @@ attn_status paged_prefill(const void* q, const void* k_pool, const void* v_pool,
   p.max_pages = max_pages;
   p.num_pages = num_pages;
   const bool masked = p.win_left >= 0 || p.win_right >= 0;
-  p.num_items = p.num_m_blocks * B * Hq;
+  p.num_items = p.num_m_blocks * B * p.units;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;
   return finish_launch(launch_prefill(p, grid, d, bf16 ? kDtBF16 : kDtF16, masked, score_xf(p), stream, g_last_name,
                                       sizeof(g_last_name)));
@@ -672,21 +713,24 @@ size_t attn_paged_workspace_bytes(int B, int Lq, int Hq, int d, int num_splits) 
   return static_cast<size_t>(num_splits) * rows * (static_cast<size_t>(d) + 1) * sizeof(float);
 }
 
-attn_status attn_dense_schedule(int B, int Hq, int Lq, int Lk, const attn_opts* opts, int grid,
-                                int32_t* off, int32_t* item) {
-  if (B <= 0 || Hq <= 0 || Lq <= 0 || Lk < 0 || grid <= 0 || off == nullptr || item == nullptr)
+attn_status attn_dense_schedule(int B, int Hq, int Hkv, int Lq, int Lk, const attn_opts* opts,
+                                int grid, int32_t* off, int32_t* item) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Lq <= 0 || Lk < 0 || grid <= 0 ||
+      off == nullptr || item == nullptr)
     return ATTN_ERR_INVALID;
-  const int64_t n = static_cast<int64_t>(m_blocks(Lq)) * B * Hq;
-  if (n > kSchedMaxItems) return ATTN_ERR_UNSUPPORTED;
   PrefillParams p;
   memset(&p, 0, sizeof(p));
+  set_pack(p, Hq, Hkv);
+  const int64_t n = static_cast<int64_t>(m_blocks(Lq, p.pack)) * B * p.units;
+  if (n > kSchedMaxItems) return ATTN_ERR_UNSUPPORTED;
   p.B = B;
   p.Hq = Hq;
+  p.Hkv = Hkv;
   p.Lq = Lq;
   p.Lk = Lk;
   resolve_window(opts, &p.win_left, &p.win_right);
   p.top_left = (opts != nullptr && opts->top_left) ? 1 : 0;
-  p.num_m_blocks = m_blocks(Lq);
+  p.num_m_blocks = m_blocks(Lq, p.pack);
   p.num_items = static_cast<int>(n);
   if (!schedule_applies(p, grid)) return ATTN_ERR_UNSUPPORTED;
   const auto s = dense_schedule(p, grid);

@@ -60,8 +60,16 @@ struct PrefillParams {
   const float* sink;               // [Hq] or nullptr
   int B, Hq, Hkv, Lq, Lk;          // batch-mode lengths (ignored for varlen)
   int total_q, total_k;            // varlen: packed extents (sequences are clamped to them)
-  int num_m_blocks;                // 256-row query blocks per (b, h)
-  int num_items;                   // num_m_blocks * B * Hq work items
+  // Query heads per work item (PackGQA): 1, or g = Hq / Hkv when the g query
+  // heads of a kv head share every tile.  A 128-row tile then holds
+  // qpt = 128 / pack queries of each of the pack heads, head-major (row
+  // r <-> head h0 + (r >> qpt_log2), query m0 + (r & (qpt - 1))), as one
+  // TMA box {d, qpt queries, pack heads} lands them.
+  int pack;
+  int qpt_log2;                    // log2(queries per 128-row tile)
+  int units;                       // Hq / pack: head groups per batch
+  int num_m_blocks;                // query blocks (two tiles) per (b, head group)
+  int num_items;                   // num_m_blocks * B * units work items
   float scale_log2;                // scale * log2(e)
   float scale;                     // plain scale (soft-cap path)
   float softcap;                   // cap (> 0 when the soft-cap variant runs)

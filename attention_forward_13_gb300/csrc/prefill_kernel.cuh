@@ -44,6 +44,13 @@
 #include <cstring>
 #include <type_traits>
 
+// L2 eviction priorities: Q tiles and O rows are touched once per launch
+// (evict first); K/V tiles are re-read by every query block of their head
+// (evict last), so the streaming Q and O do not push them out of L2.
+#ifndef ATTN_L2_HINTS
+#define ATTN_L2_HINTS 1
+#endif
+
 namespace attn {
 
 template <int D_, int DT_ = kDtBF16>
@@ -61,13 +68,23 @@ struct PrefillCfg {
   // FP8: V widened to fp16 (two 64-column atoms per tile), double-buffered.
   static constexpr int NVC = FP8 ? 2 : 1;
   static constexpr int VC_BYTES = FP8 ? BN * D * 2 : 16;
-  // Three full warpgroups: the third (warps 8-11: TMA, MMA, two idle or, for
-  // FP8, widening V) gives registers to the two softmax warpgroups with
-  // setmaxnreg (launch: 384 x 168 = 64512 registers; after: 256 x 192 +
-  // 128 x 120 = 64512).  The MMA warp's issue rate limits the step time, so
-  // it keeps enough registers not to spill (measured: 192/120 beats 200/96,
-  // 184/136 and 176/152 on the dense causal workloads).
-  static constexpr int THREADS = 384;
+  static constexpr int SOFT_WARPS = 8;            // softmax warps (two query tiles of 4)
+  static constexpr int WARP_TMA = SOFT_WARPS;     // then the producer, the MMA issuer
+  static constexpr int WARP_MMA = SOFT_WARPS + 1;  // and two more warps (FP8: V widening)
+  // The third warpgroup (the producer, MMA and two spare warps) gives
+  // registers to the two softmax warpgroups with setmaxnreg (launch: 384 x
+  // 168 = 64512 registers; after: 256 x 192 + 128 x 120 = 64512).  The MMA
+  // warp's issue rate limits the step time, so it keeps enough registers not
+  // to spill (measured: 192/120 beats 200/96, 184/136 and 176/152 on the
+  // dense causal workloads).  The host checks the launch count before the
+  // first launch (launch_prefill_t): a split above the launch total would
+  // leave setmaxnreg.inc waiting.
+  static constexpr int THREADS = 32 * (SOFT_WARPS + 4);
+  static constexpr int LAUNCH_REGS = 168;
+  static constexpr int SOFT_REGS = 192;
+  static constexpr int OTHER_REGS = 120;
+  static_assert(SOFT_WARPS * 32 * SOFT_REGS + 128 * OTHER_REGS <= THREADS * LAUNCH_REGS,
+                "register split exceeds the launch total");
   static constexpr uint32_t TM_COLS = 512;
   // Tensor-memory columns: S/P of tile t at 128*t, O of tile t at 256 + D*t.
   __device__ static constexpr uint32_t tm_s(int t) { return 128u * t; }
@@ -101,7 +118,7 @@ struct PrefillSmem : PrefillSmemFp8<C> {
   int abort_flag;
   // Epilogue staging, one 32-row x 64-byte block per softmax warp: rows go
   // in from the thread that owns them and out as 64-byte row pieces.
-  alignas(128) uint4 ostage[8][32 * 4];
+  alignas(128) uint4 ostage[C::SOFT_WARPS][32 * 4];
   // Group-mode / paged work order (order_items): slots heaviest first, each
   // slot's cost while sorting, per-cost bucket cursors, slots in use.
   uint16_t slot_order[kMaxSlots];
@@ -110,49 +127,54 @@ struct PrefillSmem : PrefillSmemFp8<C> {
   int n_slots;
 };
 
-// Maximum of 128 values: a tree of 3-input max instructions (64 instructions,
-// depth 5).
-__device__ __forceinline__ float max128(const float* v) {
-  float m[43];
+// Maximum of N values: a tree of 3-input max instructions (N = 128: 64
+// instructions, depth 5).
+template <int N>
+__device__ __forceinline__ float max_n(const float* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else if constexpr (N == 2) {
+    return fmaxf(v[0], v[1]);
+  } else if constexpr (N == 3) {
+    return fmax3(v[0], v[1], v[2]);
+  } else {
+    constexpr int M = (N + 2) / 3;
+    float m[M];
 #pragma unroll
-  for (int i = 0; i < 42; ++i) m[i] = fmax3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
-  m[42] = fmaxf(v[126], v[127]);
-  float n[15];
-#pragma unroll
-  for (int i = 0; i < 14; ++i) n[i] = fmax3(m[3 * i], m[3 * i + 1], m[3 * i + 2]);
-  n[14] = m[42];
-  float o[5];
-#pragma unroll
-  for (int i = 0; i < 5; ++i) o[i] = fmax3(n[3 * i], n[3 * i + 1], n[3 * i + 2]);
-  return fmaxf(fmax3(o[0], o[1], o[2]), fmaxf(o[3], o[4]));
+    for (int i = 0; i < M; ++i)
+      m[i] = 3 * i + 2 < N ? fmax3(v[3 * i], v[3 * i + 1], v[3 * i + 2])
+                           : (3 * i + 1 < N ? fmaxf(v[3 * i], v[3 * i + 1]) : v[3 * i]);
+    return max_n<M>(m);
+  }
 }
 
-// P for one row: p_c = 2^(s_c * a - b) for c < 128 (a = scale*log2e, or
+// P for one row: p_c = 2^(s_c * a - b) for c < 2 NP (a = scale*log2e, or
 // cap*log2e when s holds tanh values), the FMA done two lanes at a time,
 // packed to bf16/fp16 pairs, with 4 packed partial sums (8 lanes).  A masked
 // score is -inf and gives p = 0 exactly.
-template <bool BF16, int I = 0>
+template <bool BF16, int NP, int I = 0>
 __device__ __forceinline__ void exp_pack_row(const float* s, uint64_t a2, uint64_t nb2,
                                              uint32_t* pk, uint64_t* acc2) {
-  if constexpr (I < 64) {
+  if constexpr (I < NP) {
     float x0, x1;
     f2_unpack(f2_fma(f2_pack(s[2 * I], s[2 * I + 1]), a2, nb2), x0, x1);
     const float p0 = ex2_approx(x0);
     const float p1 = ex2_approx(x1);
     acc2[I & 3] = f2_add(acc2[I & 3], f2_pack(p0, p1));
     pk[I] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
-    exp_pack_row<BF16, I + 1>(s, a2, nb2, pk, acc2);
+    exp_pack_row<BF16, NP, I + 1>(s, a2, nb2, pk, acc2);
   }
 }
 
-// tanh of 128 scaled scores in place: tanh(y) = 1 - 2 / (2^(2 y log2 e) + 1),
+// tanh of N scaled scores in place: tanh(y) = 1 - 2 / (2^(2 y log2 e) + 1),
 // the multiplies, adds and FMA two lanes at a time.
-__device__ __forceinline__ void tanh128(float* s, float in_scale) {
+template <int N>
+__device__ __forceinline__ void tanh_n(float* s, float in_scale) {
   const uint64_t k2 = f2_pack(in_scale * 2.0f * kLog2e, in_scale * 2.0f * kLog2e);
   const uint64_t one2 = f2_pack(1.0f, 1.0f);
   const uint64_t m2 = f2_pack(-2.0f, -2.0f);
 #pragma unroll
-  for (int i = 0; i < 64; ++i) {
+  for (int i = 0; i < N / 2; ++i) {
     float e0, e1;
     f2_unpack(f2_mul(f2_pack(s[2 * i], s[2 * i + 1]), k2), e0, e1);
     e0 = ex2_approx(e0);
@@ -189,13 +211,14 @@ __device__ __forceinline__ void widen_v_tile(const uint8_t* raw, uint8_t* out, i
 }
 
 // Elementwise bias (Composable Kernel bias kargs).  One row's segment for a
-// K/V tile (128 keys) is loaded into registers a step ahead, raw: 16-byte
-// loads where all 8 keys are valid, element loads at the tail (keys past the
-// end read as 0; they are masked later).
-__device__ __forceinline__ void load_bias_regs(uint4 (&bn)[16], const void* src, int nvalid) {
+// K/V tile (8 NC keys: the thread's score columns) is loaded into registers
+// a step ahead, raw: 16-byte loads where all 8 keys are valid, element loads
+// at the tail (keys past the end read as 0; they are masked later).
+template <int NC>
+__device__ __forceinline__ void load_bias_regs(uint4 (&bn)[NC], const void* src, int nvalid) {
   const uint16_t* b = reinterpret_cast<const uint16_t*>(src);
 #pragma unroll
-  for (int c8 = 0; c8 < 16; ++c8) {
+  for (int c8 = 0; c8 < NC; ++c8) {
     if (8 * c8 + 8 <= nvalid) {
       bn[c8] = __ldg(reinterpret_cast<const uint4*>(b + 8 * c8));
     } else {
@@ -240,8 +263,10 @@ __device__ __forceinline__ bool wait_raw(uint64_t* bar, uint32_t parity, uint64_
   return true;
 }
 
-// One unit of work: a 256-row query block (two 128-row tiles) of one
-// (batch, query head) against all of its keys.
+// One unit of work: a query block of two 128-row tiles against all of its
+// keys.  Without packing a tile is 128 queries of query head h; with PackGQA
+// (FlashAttention-3 epilogue, PackGQA row <-> (head, query) mapping) it is
+// 128 / g queries of each of the g query heads h .. h + g - 1 of kv head hk.
 struct PrefillItem {
   int b, h, hk, rq0, rk0, bcoord, Lq, Lk, m0;
   int jb;     // first K/V tile of the item
@@ -261,7 +286,7 @@ struct PrefillItem {
 template <class C>
 __device__ __forceinline__ void load_paged_tile(const PrefillParams& p, const PrefillItem& it,
                                                 int key0, const CUtensorMap* map, uint8_t* dst,
-                                                uint64_t* bar) {
+                                                uint64_t* bar, uint64_t pol) {
   const int P = p.page_size;
   const int BR = P < C::BN ? P : C::BN;  // rows per box
   const int32_t* bt = p.block_table + static_cast<int64_t>(it.b) * p.max_pages;
@@ -278,8 +303,12 @@ __device__ __forceinline__ void load_paged_tile(const PrefillParams& p, const Pr
         atomicOr(p.err, 1u << kErrPrefillBadPage);
     }
 #pragma unroll
-    for (int c = 0; c < C::NCHUNK; ++c)
-      tma_load_3d(dst + c * C::CHUNK_BYTES + r0 * 128, map, bar, c * C::ATOM, it.hk, row);
+    for (int c = 0; c < C::NCHUNK; ++c) {
+      if constexpr (ATTN_L2_HINTS)
+        tma_load_3d_hint(dst + c * C::CHUNK_BYTES + r0 * 128, map, bar, c * C::ATOM, it.hk, row, pol);
+      else
+        tma_load_3d(dst + c * C::CHUNK_BYTES + r0 * 128, map, bar, c * C::ATOM, it.hk, row);
+    }
   }
 }
 
@@ -290,9 +319,9 @@ __device__ __forceinline__ void load_paged_tile(const PrefillParams& p, const Pr
 // from the left/right window): i + (Lk - Lq) - win_left <= j <= i + (Lk - Lq)
 // + win_right, a negative bound meaning unbounded; causal is win_right = 0.
 template <int BM, int BN, bool MASK>
-__device__ __forceinline__ bool decode_pair(const PrefillParams& p, int b, int mb, int h,
+__device__ __forceinline__ bool decode_pair(const PrefillParams& p, int b, int mb, int unit,
                                             PrefillItem& it) {
-  it.h = h;
+  it.h = unit * p.pack;  // first query head of the item
   it.b = b;
   it.hk = it.h / (p.Hq / p.Hkv);
   it.Lq = p.Lq;
@@ -314,16 +343,17 @@ __device__ __forceinline__ bool decode_pair(const PrefillParams& p, int b, int m
   } else if (p.seqlens_k != nullptr) {  // paged KV cache: per-sequence key count
     it.Lk = max(0, min(p.seqlens_k[it.b], p.max_pages * p.page_size));
   }
-  it.m0 = mb * 2 * BM;
+  const int qpt = 1 << p.qpt_log2;  // queries per tile (BM without packing)
+  it.m0 = mb * 2 * qpt;
   if (it.m0 >= it.Lq) return false;
   const int diag = p.top_left ? 0 : it.Lk - it.Lq;  // key on row 0's diagonal
   int tb[2], te[2];  // K/V tile range [tb, te) of each query tile
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int mt = it.m0 + t * BM;
+    const int mt = it.m0 + t * qpt;
     tb[t] = te[t] = 0;
     if (mt < it.Lq) {
-      const int last = min(mt + BM - 1, it.Lq - 1);
+      const int last = min(mt + qpt - 1, it.Lq - 1);
       int kend = it.Lk, kbeg = 0;  // keys [kbeg, kend) some row of the tile keeps
       if (MASK && p.win_right >= 0) kend = min(it.Lk, last + diag + p.win_right + 1);
       if (MASK && p.win_left >= 0) kbeg = max(0, mt + diag - p.win_left);
@@ -351,7 +381,7 @@ __device__ __forceinline__ bool decode_pair(const PrefillParams& p, int b, int m
 // paged cache the sequences differ in length, so that order leaves holes
 // (blocks past a short sequence's end) and mixes costs; there every CTA sorts
 // the (query block, sequence) slots by their K/V step count, heaviest first,
-// and items become (slot, head) in that order.
+// and items become (slot, head group) in that order.
 struct ItemOrder {
   const uint16_t* slot;  // slot = query block * B + sequence, heaviest first
   int n;                 // slots in use; -1: plain order
@@ -362,18 +392,18 @@ __device__ __forceinline__ bool decode_item(const PrefillParams& p, const ItemOr
                                             PrefillItem& it) {
   if constexpr (ORD) {
     if (ord.n >= 0) {
-      const int pos = item / p.Hq;
+      const int pos = item / p.units;
       if (pos >= ord.n) return false;
       const int slot = ord.slot[pos];
       const int mb = slot / p.B;
-      return decode_pair<BM, BN, MASK>(p, slot - mb * p.B, mb, item - pos * p.Hq, it);
+      return decode_pair<BM, BN, MASK>(p, slot - mb * p.B, mb, item - pos * p.units, it);
     }
   }
-  const int nbh = p.B * p.Hq;
+  const int nbh = p.B * p.units;
   const int mb_i = item / nbh;
   const int bh = item - mb_i * nbh;
   const int mb = MASK ? (p.num_m_blocks - 1 - mb_i) : mb_i;
-  return decode_pair<BM, BN, MASK>(p, bh / p.Hq, mb, bh % p.Hq, it);
+  return decode_pair<BM, BN, MASK>(p, bh / p.units, mb, bh % p.units, it);
 }
 
 // Builds the group-mode / paged work order in shared memory; every thread of
@@ -482,7 +512,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
-      mbar_init(&sm.p_full[t], 128);
+      mbar_init(&sm.p_full[t], 128);  // every softmax thread of the tile
       mbar_init(&sm.o_final[t], 1);
       mbar_init(&sm.o_free[t], 128);
     }
@@ -490,7 +520,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == C::WARP_MMA) {
     tmem_alloc(&sm.tmem_base, C::TM_COLS);
     tmem_relinquish();
   }
@@ -505,13 +535,15 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
   const uint32_t tmem = sm.tmem_base;
   const Waiter w{globaltimer_ns() + p.timeout_ns, &sm.abort_flag, p.err};
 
-  if (warp >= 8) {
-    setmaxnreg_dec<120>();
-    if (warp == 8 && lane == 0) {
+  if (warp >= C::SOFT_WARPS) {
+    setmaxnreg_dec<C::OTHER_REGS>();
+    if (warp == C::WARP_TMA && lane == 0) {
       // ===================== TMA producer =====================================
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
+      const uint64_t pol_once = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
       int g = 0, qn = 0, k_armed = 0, v_armed = 0;
       int qa[2] = {0, 0};  // arms of each tile's q_full
       bool ok = true;
@@ -528,9 +560,14 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           mbar_arrive_expect_tx(&sm.q_full[t], C::TILE_BYTES);
           ++qa[t];
 #pragma unroll
-          for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_4d(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full[t], c * C::ATOM,
-                        it.rq0 + it.m0 + t * C::BM, it.h, it.bcoord);
+          for (int c = 0; c < C::NCHUNK; ++c) {  // box {ATOM, qpt queries, pack heads}
+            if constexpr (ATTN_L2_HINTS)
+              tma_load_4d_hint(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full[t], c * C::ATOM,
+                               it.rq0 + it.m0 + (t << p.qpt_log2), it.h, it.bcoord, pol_once);
+            else
+              tma_load_4d(sm.q[t] + c * C::CHUNK_BYTES, &p.tm_q, &sm.q_full[t], c * C::ATOM,
+                          it.rq0 + it.m0 + (t << p.qpt_log2), it.h, it.bcoord);
+          }
         }
         if (!ok) break;
         ++qn;
@@ -540,23 +577,37 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           if (!(ok = w.wait(&sm.k_empty[s], ph ^ 1, kErrPrefillKEmpty))) break;
           mbar_arrive_expect_tx(&sm.k_full[s], C::TILE_BYTES);
           if (p.block_table != nullptr) {
-            load_paged_tile<C>(p, it, (it.jb + j) * C::BN, &p.tm_k, sm.k[s], &sm.k_full[s]);
+            load_paged_tile<C>(p, it, (it.jb + j) * C::BN, &p.tm_k, sm.k[s], &sm.k_full[s],
+                               pol_kv);
           } else {
 #pragma unroll
-            for (int c = 0; c < C::NCHUNK; ++c)
-              tma_load_4d(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s], c * C::ATOM,
-                          it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
+            for (int c = 0; c < C::NCHUNK; ++c) {
+              if constexpr (ATTN_L2_HINTS)
+                tma_load_4d_hint(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s],
+                                 c * C::ATOM, it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord,
+                                 pol_kv);
+              else
+                tma_load_4d(sm.k[s] + c * C::CHUNK_BYTES, &p.tm_k, &sm.k_full[s],
+                            c * C::ATOM, it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
+            }
           }
           ++k_armed;
           if (!(ok = w.wait(&sm.v_empty[s], ph ^ 1, kErrPrefillVEmpty))) break;
           mbar_arrive_expect_tx(&sm.v_full[s], C::TILE_BYTES);
           if (p.block_table != nullptr) {
-            load_paged_tile<C>(p, it, (it.jb + j) * C::BN, &p.tm_v, sm.v[s], &sm.v_full[s]);
+            load_paged_tile<C>(p, it, (it.jb + j) * C::BN, &p.tm_v, sm.v[s], &sm.v_full[s],
+                               pol_kv);
           } else {
 #pragma unroll
-            for (int c = 0; c < C::NCHUNK; ++c)
-              tma_load_4d(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s], c * C::ATOM,
-                          it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
+            for (int c = 0; c < C::NCHUNK; ++c) {
+              if constexpr (ATTN_L2_HINTS)
+                tma_load_4d_hint(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s],
+                                 c * C::ATOM, it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord,
+                                 pol_kv);
+              else
+                tma_load_4d(sm.v[s] + c * C::CHUNK_BYTES, &p.tm_v, &sm.v_full[s],
+                            c * C::ATOM, it.rk0 + (it.jb + j) * C::BN, it.hk, it.bcoord);
+            }
           }
           ++v_armed;
         }
@@ -573,7 +624,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         for (int jj = max(0, v_armed - C::NS); jj < v_armed; ++jj)
           wait_raw(&sm.v_full[jj % C::NS], (jj / C::NS) & 1, dl);
       }
-    } else if (warp == 9) {
+    } else if (warp == C::WARP_MMA) {
       // ===================== MMA issuer (whole warp) ==========================
       // Every lane runs the loop (so its operand arithmetic stays warp-uniform)
       // and waits on the barriers itself; only the elected lane issues MMAs and
@@ -609,7 +660,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         if constexpr (FP8) vd = sdesc_sw128(smem_u32(sm.vc[g % C::NVC]), C::CHUNK_BYTES, 1024);
         else vd = vdesc0 + static_cast<uint64_t>((g % C::NS) * kTileDesc);
 #pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k) {
+        for (int k = 0; k < C::BN / 16; ++k) {  // 16 keys per MMA
           umma_ts_warp(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8, vd + ((k * 16 * 128) >> 4),
                        idesc_o, (acc || k > 0) ? 1u : 0u, lead);
         }
@@ -686,12 +737,12 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       umma_commit_warp(&sm.teardown, lead);
       if (!wait_raw(&sm.teardown, 0, globaltimer_ns() + 50000000ull) && p.err)
         atomicOr(p.err, 1u << kErrPrefillTeardown);
-    } else if (warp == 10 || warp == 11) {
+    } else if (warp == C::WARP_MMA + 1 || warp == C::WARP_MMA + 2) {
       if constexpr (FP8) {
       // ============== FP8: widen each V tile from e4m3 to fp16 ================
       // (the P.V MMA runs on the fp16 tensor path: its operands must share
       // one type, and P keeps more precision than e4m3 that way).
-      const int ct = threadIdx.x - 320;  // 0..63
+      const int ct = threadIdx.x - 32 * (C::WARP_MMA + 1);  // 0..63
       int g = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
@@ -715,11 +766,14 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
     }
     // the other lanes: no role
   } else {
-    setmaxnreg_inc<192>();
+    setmaxnreg_inc<C::SOFT_REGS>();
     // ======================= softmax warpgroups =============================
+    // Warps 4t .. 4t+3 run query tile t, thread = row = TMEM lane (warp & 3
+    // picks the lane quarter).
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-    const int t = warp >> 2;          // query tile of this warpgroup
-    const int r = threadIdx.x & 127;  // row within the tile == TMEM lane
+    constexpr int W = C::BN;                          // score columns per thread per step
+    const int t = warp >> 2;                          // query tile of this warp
+    const int r = (warp & 3) * 32 + lane;             // row within the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + C::tm_s(t) + lane_base;
     const uint32_t tO = tmem + C::tm_o(t) + lane_base;
@@ -730,17 +784,19 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       if (item >= p.num_items) break;
       PrefillItem it;
       if (!decode_item<C::BM, C::BN, MASK, ORD>(p, ord, item, it)) continue;
-      const int mt = it.m0 + t * C::BM;
-      if (mt >= it.Lq) continue;  // this tile has no row
-      const int qi = mt + r;      // query index within the sequence
+      const int qmask = (1 << p.qpt_log2) - 1;
+      const int mt = it.m0 + (t << p.qpt_log2);  // first query of this tile
+      if (mt >= it.Lq) continue;                  // this tile has no row
+      const int qi = mt + (r & qmask);            // this row's query index within the sequence
+      const int hr = it.h + (r >> p.qpt_log2);    // and its query head
       const int nt = it.ue[t] - it.ub[t];  // K/V steps of this tile
       const int diag = p.top_left ? 0 : it.Lk - it.Lq;  // key on row 0's diagonal
-      const int last = min(mt + C::BM - 1, it.Lq - 1);
+      const int last = min(mt + qmask, it.Lq - 1);      // last query of this tile
       float alibi_raw = 0.0f;      // ALiBi slope / scale (raw-score units)
       const T* bias_row = nullptr;  // this row's bias, key 0
-      if constexpr (XF == kXfAlibi) alibi_raw = p.alibi[it.b * p.alibi_stride + it.h] * p.inv_scale;
+      if constexpr (XF == kXfAlibi) alibi_raw = p.alibi[it.b * p.alibi_stride + hr] * p.inv_scale;
       if constexpr (XF == kXfBias)
-        bias_row = reinterpret_cast<const T*>(p.bias) + it.b * p.bias_batch + it.h * p.bias_head +
+        bias_row = reinterpret_cast<const T*>(p.bias) + it.b * p.bias_batch + hr * p.bias_head +
                    static_cast<int64_t>(qi) * p.bias_row;
 
       float m_use = -INFINITY;  // exp2 subtrahend currently in use (log2 units)
@@ -748,17 +804,19 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       // Bias: this row's segment for the coming K/V tile, loaded right after
       // the previous step's P is handed over, so that the loads run while the
       // tensor core computes the next S; the L2 is warmed one step further
-      // ahead (the valid bytes only: up to three 128-byte lines).
-      uint4 bn[16];
+      // ahead (the valid bytes only).
+      uint4 bn[W / 8];
       auto fetch_bias = [&](int jj) {  // registers for step jj, L2 for step jj + 1
         const int k0 = (it.jb + it.ub[t] + jj) * C::BN;
-        load_bias_regs(bn, bias_row + k0, it.Lk - k0);
+        load_bias_regs<W / 8>(bn, bias_row + k0, it.Lk - k0);
         if (jj + 1 < nt) {
           const char* nb = reinterpret_cast<const char*>(bias_row + k0 + C::BN);
-          const int bytes = min(it.Lk - (k0 + C::BN), C::BN) * static_cast<int>(sizeof(T));
-          prefetch_l2(nb);
-          if (bytes > 128) prefetch_l2(nb + 128);
-          prefetch_l2(nb + bytes - 1);
+          const int bytes = min(it.Lk - (k0 + C::BN), W) * static_cast<int>(sizeof(T));
+          if (bytes > 0) {
+            prefetch_l2(nb);
+            if (bytes > 128) prefetch_l2(nb + 128);
+            prefetch_l2(nb + bytes - 1);
+          }
         }
       };
       if constexpr (XF == kXfBias)
@@ -768,40 +826,26 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         if (!ok) break;
         ++pc;
         tc_fence_after();
-        uint32_t sr[128];
-        {
-          uint32_t (&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-          uint32_t (&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-          uint32_t (&a2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
-          uint32_t (&a3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
-          if constexpr (XF == kXfBias) {
-            // A quarter of the scores at a time, each taking its bias from
-            // registers as it lands, so that the prefetched segment and the
-            // scores are never all live at once.
-            tmem_ld32(tS + 0, a0);
+        uint32_t sr[W];
+        if constexpr (XF == kXfBias) {
+          // A quarter of 32 scores at a time, each taking its bias from
+          // registers as it lands, so that the prefetched segment and the
+          // scores are never all live at once.
+#pragma unroll
+          for (int qq = 0; qq < W / 32; ++qq) {
+            uint32_t (&aq)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * qq]);
+            tmem_ld32(tS + 32 * qq, aq);
             tmem_ld_wait();
-            reg_fence(a0);
-            if (qi < it.Lq) add_bias_quarter<BF16>(reinterpret_cast<float*>(&sr[0]), &bn[0], p.inv_scale);
-            tmem_ld32(tS + 32, a1);
-            tmem_ld_wait();
-            reg_fence(a1);
-            if (qi < it.Lq) add_bias_quarter<BF16>(reinterpret_cast<float*>(&sr[32]), &bn[4], p.inv_scale);
-            tmem_ld32(tS + 64, a2);
-            tmem_ld_wait();
-            reg_fence(a2);
-            if (qi < it.Lq) add_bias_quarter<BF16>(reinterpret_cast<float*>(&sr[64]), &bn[8], p.inv_scale);
-            tmem_ld32(tS + 96, a3);
-            tmem_ld_wait();
-            reg_fence(a3);
-            if (qi < it.Lq) add_bias_quarter<BF16>(reinterpret_cast<float*>(&sr[96]), &bn[12], p.inv_scale);
-          } else {
-            tmem_ld32(tS + 0, a0);
-            tmem_ld32(tS + 32, a1);
-            tmem_ld32(tS + 64, a2);
-            tmem_ld32(tS + 96, a3);
-            tmem_ld_wait();
-            reg_fence(sr);
+            reg_fence(aq);
+            if (qi < it.Lq)
+              add_bias_quarter<BF16>(reinterpret_cast<float*>(&sr[32 * qq]), &bn[4 * qq], p.inv_scale);
           }
+        } else {
+#pragma unroll
+          for (int qq = 0; qq < W / 32; ++qq)
+            tmem_ld32(tS + 32 * qq, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * qq]));
+          tmem_ld_wait();
+          reg_fence(sr);
         }
         // Raw scores in place; the soft-cap variant turns them into tanh
         // values whose log2-unit score is cap*log2(e)*s, else scale*log2(e)
@@ -810,7 +854,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         float a_coef = p.scale_log2;
         const int j0 = (it.jb + it.ub[t] + j) * C::BN;  // first key of this K/V tile
         if constexpr (XF == kXfSoftcap) {
-          tanh128(s, p.scale * p.softcap_inv);
+          tanh_n<W>(s, p.scale * p.softcap_inv);
           a_coef = p.softcap * kLog2e;
         } else if constexpr (XF == kXfAlibi) {
           // CK ALiBi position encoding (slope per (batch, head), aligned like
@@ -821,42 +865,40 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           // below 2^24, so the subtraction is exact.
           const int dq = qi + diag - j0;  // this row's diagonal, as a column
           const float fdq = static_cast<float>(dq);
-          if (dq >= C::BN - 1 || dq <= 0) {
-            // The whole tile is on one side of the diagonal: -slope*|dq - c|
-            // is +-slope*(c - dq), two packed operations per pair of scores
+          if (dq >= W - 1 || dq <= 0) {
+            // All columns on one side of the diagonal: -slope*|dq - c| is
+            // +-slope*(c - dq), two packed operations per pair of scores
             // (an exact subtraction, then the same single-rounding FMA).
             const float k = dq > 0 ? alibi_raw : -alibi_raw;
             const uint64_t k2 = f2_pack(k, k), nq2 = f2_pack(-fdq, -fdq);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
+            for (int i = 0; i < W / 2; ++i) {
               const uint64_t d2 = f2_add(f2_pack(static_cast<float>(2 * i), static_cast<float>(2 * i + 1)), nq2);
               f2_unpack(f2_fma(k2, d2, f2_pack(s[2 * i], s[2 * i + 1])), s[2 * i], s[2 * i + 1]);
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
+            for (int c = 0; c < W; ++c)
               s[c] = fmaf(-alibi_raw, fabsf(fdq - static_cast<float>(c)), s[c]);
           }
-        } else if constexpr (XF == kXfBias) {
-          // CK elementwise bias (natural-log units, added to the scaled score).
-          // Composable Kernel elementwise bias (natural-log units, added to the
-          // scaled score): added above, as the scores left tensor memory.
         }
-        if ((j0 + C::BN > it.Lk) ||
-            (MASK && p.win_right >= 0 && j0 + C::BN - 1 > mt + diag + p.win_right) ||
+        // (The elementwise bias was added above, as the scores left tensor
+        // memory.)
+        if ((j0 + W > it.Lk) ||
+            (MASK && p.win_right >= 0 && j0 + W - 1 > mt + diag + p.win_right) ||
             (MASK && p.win_left >= 0 && j0 < last + diag - p.win_left)) {
           int hi = it.Lk - 1 - j0, lo = 0;  // kept columns [lo, hi] of this row
           if (MASK && p.win_right >= 0) hi = min(hi, qi + diag + p.win_right - j0);
           if (MASK && p.win_left >= 0) lo = qi + diag - p.win_left - j0;
-          if (lo <= 0) {  // no left bound inside the tile (plain causal or the tail)
+          if (lo <= 0) {  // no left bound inside the columns (plain causal or the tail)
 #pragma unroll
-            for (int c = 0; c < 128; ++c) s[c] = c <= hi ? s[c] : -INFINITY;
+            for (int c = 0; c < W; ++c) s[c] = c <= hi ? s[c] : -INFINITY;
           } else {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : -INFINITY;
+            for (int c = 0; c < W; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : -INFINITY;
           }
         }
-        const float m_new = fmaxf(m_use, max128(s) * a_coef);  // a_coef > 0: order kept
+        const float m_new = fmaxf(m_use, max_n<W>(s) * a_coef);  // a_coef > 0: order kept
         float alpha = 1.0f;
         if (m_new - m_use > 8.0f) {  // false when both are -inf (NaN compare)
           alpha = ex2_approx(m_use - m_new);
@@ -864,13 +906,15 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         }
         const float msub = (m_use == -INFINITY) ? 0.0f : m_use;
         uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f in both lanes
-        uint32_t pk[64];
-        exp_pack_row<BF16>(s, f2_pack(a_coef, a_coef), f2_pack(-msub, -msub), pk, acc2);
+        uint32_t pk[W / 2];
+        exp_pack_row<BF16, W / 2>(s, f2_pack(a_coef, a_coef), f2_pack(-msub, -msub), pk, acc2);
         float r0, r1;
         f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), r0, r1);
         l = l * alpha + (r0 + r1);
-        tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        // P over the first W/2 columns of S.
+#pragma unroll
+        for (int qq = 0; qq < W / 64; ++qq)
+          tmem_st32(tS + 32 * qq, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * qq]));
         // The P.V MMA of the previous K/V tile finished before this S was
         // produced (its commit covers every earlier MMA), so O can be
         // rescaled now.
@@ -907,9 +951,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         tc_fence_after();
       }
       const float msub = (m_use == -INFINITY) ? 0.0f : m_use;
-      float mfin = msub, ltot = l, oscale;
+      const bool row_ok = qi < it.Lq;
+      float oscale;  // 1 / denominator (with the sink's share)
+      float mfin = msub, ltot = l;
       if (p.sink != nullptr) {
-        const float sl = p.sink[it.h] * kLog2e;
+        const float sl = p.sink[hr] * kLog2e;
         if (l > 0.0f) {
           mfin = fmaxf(msub, sl);
           const float a = ex2_approx(msub - mfin);
@@ -923,29 +969,33 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       } else {
         oscale = (l > 0.0f) ? 1.0f / l : 0.0f;
       }
-      const bool row_ok = qi < it.Lq;
-      if (row_ok && p.lse != nullptr) {
-        const float lse = (ltot > 0.0f) ? (mfin + __log2f(ltot)) * kLn2 : -INFINITY;
-        p.lse[it.b * p.lse_batch + it.h * p.lse_head + it.rq0 + qi] = lse;
-      }
+      const float lse_out = (ltot > 0.0f) ? (mfin + __log2f(ltot)) * kLn2 : -INFINITY;  // natural log
+      if (row_ok && p.lse != nullptr)
+        p.lse[it.b * p.lse_batch + hr * p.lse_head + it.rq0 + qi] = lse_out;
       constexpr int OB = FP8 ? 1 : 2;  // bytes per output element
-      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) +
-                       (it.b * p.o_batch + it.h * p.o_head +
-                        static_cast<int64_t>(it.rq0 + mt + (warp & 3) * 32) * p.o_row) * OB;
-      const int rows_left = it.Lq - (mt + (warp & 3) * 32);  // valid rows of this warp
+      // Output row of tile row R (its head and query; valid while the query
+      // is inside the sequence).
+      auto orow = [&](int R, bool& valid) -> uint8_t* {
+        const int q = mt + (R & qmask);
+        valid = q < it.Lq;
+        return reinterpret_cast<uint8_t*>(p.o) +
+               (it.b * p.o_batch + static_cast<int64_t>(it.h + (R >> p.qpt_log2)) * p.o_head +
+                static_cast<int64_t>(it.rq0 + q) * p.o_row) * OB;
+      };
       if (have_o) {
-        // O is read from tensor memory first; then 64 bytes of each row per
-        // round (32 fp16/bf16 or 64 e4m3 columns): each thread packs its row
-        // into the stage (16-byte pieces, XOR-swizzled by row pair so 8
-        // consecutive rows hit distinct banks), then the warp writes 8 rows x
-        // 64 contiguous bytes per instruction instead of 32 scattered 16-byte
-        // pieces.
+        // O is read from tensor memory first (one wait) and goes back to the
+        // MMA warp before any packing or store; then 64 bytes of each row
+        // per round (32 fp16/bf16 or 64 e4m3 columns): each thread packs its
+        // row into the stage (16-byte pieces, XOR-swizzled by row pair so 8
+        // consecutive rows hit distinct banks), then the warp writes 8 rows
+        // x 64 contiguous bytes per instruction instead of 32 scattered
+        // 16-byte pieces.
         constexpr int RC = 64 / OB;  // columns per round
-        uint4* stage = sm.ostage[warp & 7];
-        const int lr = lane & 31;
+        uint4* stage = sm.ostage[warp];
+        const int lr = lane;
+        const uint64_t pol_o = l2_policy_evict_first();
+        (void)pol_o;
         if constexpr (FP8) oscale *= p.o_scale;  // FP8 static quantisation: scale_p * scale_o
-        // All of O_t at once (one wait), then O_t goes back to the MMA warp
-        // before any packing or store.
         uint32_t ov[D];
 #pragma unroll
         for (int c = 0; c < D; c += 32) tmem_ld32(tO + c, *reinterpret_cast<uint32_t(*)[32]>(&ov[c]));
@@ -983,16 +1033,21 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           __syncwarp();
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const int rr = 8 * k + (lr >> 2), q = lr & 3;
-            const uint4 v4 = stage[rr * 4 + (q ^ ((rr >> 1) & 3))];
-            if (rr < rows_left)
-              *reinterpret_cast<uint4*>(obase + (static_cast<int64_t>(rr) * p.o_row + c0) * OB +
-                                        16 * q) = v4;
+            const int rw = 8 * k + (lr >> 2), q = lr & 3;
+            const uint4 v4 = stage[rw * 4 + (q ^ ((rw >> 1) & 3))];
+            bool valid;
+            uint8_t* dst = orow((warp & 3) * 32 + rw, valid);
+            if (valid) {
+              if constexpr (ATTN_L2_HINTS) st_global_v4_hint(dst + c0 * OB + 16 * q, v4, pol_o);
+              else *reinterpret_cast<uint4*>(dst + c0 * OB + 16 * q) = v4;
+            }
           }
           __syncwarp();
         }
       } else if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(obase + static_cast<int64_t>(r & 31) * p.o_row * OB);
+        bool valid;  // == row_ok
+        uint4* dst = reinterpret_cast<uint4*>(orow(r, valid));
+        (void)valid;
 #pragma unroll
         for (int i = 0; i < D * OB / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
       }
@@ -1001,7 +1056,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TM_COLS);
   }
@@ -1014,7 +1069,15 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream
   const int smem = static_cast<int>(sizeof(PrefillSmem<C>)) + 1024;
   static bool configured = false;  // per instantiation; attribute set is idempotent
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // The softmax warpgroups raise their register budget with setmaxnreg,
+    // drawing on what the block was launched with: the kernel must have been
+    // built with exactly the launch count the split assumes, else that
+    // instruction would wait forever.  Refuse to launch otherwise.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }

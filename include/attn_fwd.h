@@ -244,22 +244,28 @@ int attn_paged_window_pages(int Lq, int page_size, int max_pages_per_seq, const 
 
 /* The static work schedule attn_fwd runs for a dense problem with a causal
  * or window mask on a grid of `grid` CTAs (a load-balancing order of this
- * implementation; the pages fix none).  Work item i is query block
- * ceil(Lq/256) - 1 - i / (B*Hq) (256 rows) of batch (i % (B*Hq)) / Hq and
- * head i % Hq; CTA c runs items item[off[c]] .. item[off[c+1] - 1] in that
- * order.  The items are packed longest processing time first (cost: the
- * block's K/V tiles of 128 keys plus 4), then moved and swapped off the
- * most loaded CTA while that lowers its load; each CTA's list runs lightest
- * first.  attn_fwd launches min(SM count, items) CTAs and uses this
- * schedule exactly when this call returns ATTN_OK for that grid.
- *   off: host int32 [grid + 1]; item: host int32 [B * Hq * ceil(Lq / 256)].
+ * implementation; the pages fix none).  A work item is a query block of two
+ * 128-row tiles of one batch and one head group: with g = Hq / Hkv a power
+ * of two from 2 to 16 the g query heads of a kv head share every tile
+ * (PackGQA, FlashAttention-3 epilogue: 128 / g queries of each of the g
+ * heads), else a head group is one query head and a tile holds 128 queries.
+ * With U = Hq / (heads per group) groups and Q = 256 / (heads per group)
+ * queries per block, work item i is query block ceil(Lq / Q) - 1 - i / (B*U)
+ * of batch (i % (B*U)) / U and head group i % U; CTA c runs items
+ * item[off[c]] .. item[off[c+1] - 1] in that order.  The items are packed
+ * longest processing time first (cost: the block's K/V tiles of 128 keys
+ * plus 4), then moved and swapped off the most loaded CTA while that lowers
+ * its load; each CTA's list runs lightest first.  attn_fwd launches
+ * min(SM count, items) CTAs and uses this schedule exactly when this call
+ * returns ATTN_OK for that grid.
+ *   off: host int32 [grid + 1]; item: host int32 [B * U * ceil(Lq / Q)].
  *   Returns ATTN_ERR_UNSUPPORTED when the problem keeps the plain snake
  *   order (no mask, more than 1536 items or 160 CTAs, or no more items than
- *   CTAs), ATTN_ERR_INVALID for non-positive sizes or NULL buffers.  Host
- *   only: needs no device.  opts as for attn_fwd (only the mask fields are
- *   read); may be NULL. */
-attn_status attn_dense_schedule(int B, int Hq, int Lq, int Lk, const attn_opts* opts, int grid,
-                                int32_t* off, int32_t* item);
+ *   CTAs), ATTN_ERR_INVALID for non-positive sizes, Hq % Hkv != 0 or NULL
+ *   buffers.  Host only: needs no device.  opts as for attn_fwd (only the
+ *   mask fields are read); may be NULL. */
+attn_status attn_dense_schedule(int B, int Hq, int Hkv, int Lq, int Lk, const attn_opts* opts,
+                                int grid, int32_t* off, int32_t* item);
 
 /* Human-readable name of a status. */
 const char* attn_status_string(attn_status status);

@@ -18,17 +18,18 @@ import attention_forward_13_gb300 as A
 GRID = 152
 
 
-def block_steps(Lq, Lk, mb, wl, wr, top_left):
+def block_steps(Lq, Lk, mb, wl, wr, top_left, qpt=128):
     """K/V tiles (128 keys) from the first to the last one that some row of
-    the block's two 128-row tiles keeps a key in."""
+    the block's two tiles keeps a key in; a tile covers qpt queries (128, or
+    128 / g with g query heads packed per tile)."""
     diag = 0 if top_left else Lk - Lq
     lo, hi = None, None
     j = np.arange(Lk)
     for t in range(2):
-        r0 = mb * 256 + t * 128
+        r0 = mb * 2 * qpt + t * qpt
         if r0 >= Lq:
             continue
-        rows = np.arange(r0, min(r0 + 128, Lq))[:, None] + diag
+        rows = np.arange(r0, min(r0 + qpt, Lq))[:, None] + diag
         keep = np.ones((rows.shape[0], Lk), dtype=bool)
         if wr >= 0:
             keep &= j[None, :] <= rows + wr
@@ -42,9 +43,15 @@ def block_steps(Lq, Lk, mb, wl, wr, top_left):
     return 0 if lo is None else hi - lo
 
 
-def costs(B, H, Lq, Lk, wl, wr, top_left):
-    nbh, M = B * H, (Lq + 255) // 256
-    per_block = [10 * block_steps(Lq, Lk, mb, wl, wr, top_left) + 40 for mb in range(M)]
+def costs(B, H, Lq, Lk, wl, wr, top_left, Hkv=None):
+    """Item costs in the documented item order: items are (query block, batch,
+    head group), a group being the g = H / Hkv heads of a kv head when g is
+    2, 4, 8 or 16 (PackGQA), else one head."""
+    g = H // (Hkv or H)
+    pack = g if g in (2, 4, 8, 16) else 1
+    qpt = 128 // pack
+    nbh, M = B * (H // pack), (Lq + 2 * qpt - 1) // (2 * qpt)
+    per_block = [10 * block_steps(Lq, Lk, mb, wl, wr, top_left, qpt) + 40 for mb in range(M)]
     return [per_block[M - 1 - i // nbh] for i in range(M * nbh)]
 
 
@@ -59,16 +66,19 @@ def snake_loads(cost, grid):
     return loads
 
 
-# B, H, Lq, Lk, causal, window (left, right), top_left
+# B, H, Hkv, Lq, Lk, causal, window (left, right), top_left
 SHAPES = [
-    (4, 16, 2048, 2048, True, None, False),
-    (8, 16, 1024, 1024, True, None, False),
-    (2, 16, 4096, 4096, True, None, False),
-    (4, 16, 2048, 2048, False, (512, 0), False),
-    (4, 16, 1000, 3000, True, None, False),
-    (2, 8, 3000, 1000, True, None, False),
-    (1, 16, 4096, 4096, False, (300, 200), True),
-    (3, 7, 2500, 2600, False, (-1, 64), False),
+    (4, 16, 16, 2048, 2048, True, None, False),
+    (8, 16, 16, 1024, 1024, True, None, False),
+    (2, 16, 16, 4096, 4096, True, None, False),
+    (4, 16, 16, 2048, 2048, False, (512, 0), False),
+    (4, 16, 16, 1000, 3000, True, None, False),
+    (2, 8, 8, 3000, 1000, True, None, False),
+    (1, 16, 16, 4096, 4096, False, (300, 200), True),
+    (3, 7, 7, 2500, 2600, False, (-1, 64), False),
+    (2, 32, 8, 2048, 2048, True, None, False),      # PackGQA g = 4: 32 queries per tile
+    (4, 16, 2, 1500, 1700, True, (200, -1), False),  # g = 8 with a window
+    (2, 12, 4, 2048, 2048, True, None, False),      # g = 3: not packed
 ]
 
 
@@ -81,10 +91,11 @@ def _wlr(causal, window):
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[str(i) for i in range(len(SHAPES))])
 def test_schedule_contract(shape):
-    B, H, Lq, Lk, causal, window, tl = shape
-    sched = A.attn_dense_schedule(B, H, Lq, Lk, GRID, causal=causal, window=window, top_left=tl)
+    B, H, Hkv, Lq, Lk, causal, window, tl = shape
+    sched = A.attn_dense_schedule(B, H, Lq, Lk, GRID, causal=causal, window=window, top_left=tl,
+                                  Hkv=Hkv)
     assert sched is not None and len(sched) == GRID
-    cost = costs(B, H, Lq, Lk, *_wlr(causal, window), tl)
+    cost = costs(B, H, Lq, Lk, *_wlr(causal, window), tl, Hkv=Hkv)
     n = len(cost)
     flat = [i for lst in sched for i in lst]
     assert sorted(flat) == list(range(n)), "every work item exactly once"
