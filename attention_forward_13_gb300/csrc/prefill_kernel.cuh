@@ -166,13 +166,15 @@ __device__ __forceinline__ void exp_pack_row(const float* s, uint64_t a2, uint64
   }
 }
 
-// tanh of N scaled scores in place: tanh(y) = 1 - 2 / (2^(2 y log2 e) + 1),
-// the multiplies, adds and FMA two lanes at a time.
+// Soft-cap in the form the softmax consumes: s <- r = 1 / (2^(2 y log2 e) + 1)
+// with y = in_scale * s, so that tanh(y) = 1 - 2 r and the capped score in
+// log2 units is c (1 - 2 r), c = cap * log2 e.  The exponent's FMA then takes
+// r directly (r * (-2c) + (c - m)) and the row maximum is c (1 - 2 min r):
+// the tanh's own final FMA disappears from the chain.
 template <int N>
-__device__ __forceinline__ void tanh_n(float* s, float in_scale) {
+__device__ __forceinline__ void softcap_r_n(float* s, float in_scale) {
   const uint64_t k2 = f2_pack(in_scale * 2.0f * kLog2e, in_scale * 2.0f * kLog2e);
   const uint64_t one2 = f2_pack(1.0f, 1.0f);
-  const uint64_t m2 = f2_pack(-2.0f, -2.0f);
 #pragma unroll
   for (int i = 0; i < N / 2; ++i) {
     float e0, e1;
@@ -181,7 +183,28 @@ __device__ __forceinline__ void tanh_n(float* s, float in_scale) {
     e1 = ex2_approx(e1);
     float d0, d1;
     f2_unpack(f2_add(f2_pack(e0, e1), one2), d0, d1);
-    f2_unpack(f2_fma(f2_pack(rcp_approx(d0), rcp_approx(d1)), m2, one2), s[2 * i], s[2 * i + 1]);
+    s[2 * i] = rcp_approx(d0);
+    s[2 * i + 1] = rcp_approx(d1);
+  }
+}
+
+// Minimum of N values (a tree of 3-input min instructions).
+template <int N>
+__device__ __forceinline__ float min_n(const float* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else if constexpr (N == 2) {
+    return fminf(v[0], v[1]);
+  } else if constexpr (N == 3) {
+    return fmin3(v[0], v[1], v[2]);
+  } else {
+    constexpr int M = (N + 2) / 3;
+    float m[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+      m[i] = 3 * i + 2 < N ? fmin3(v[3 * i], v[3 * i + 1], v[3 * i + 2])
+                           : (3 * i + 1 < N ? fminf(v[3 * i], v[3 * i + 1]) : v[3 * i]);
+    return min_n<M>(m);
   }
 }
 
@@ -847,15 +870,14 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           tmem_ld_wait();
           reg_fence(sr);
         }
-        // Raw scores in place; the soft-cap variant turns them into tanh
-        // values whose log2-unit score is cap*log2(e)*s, else scale*log2(e)
-        // is folded into the exponent's FMA (CK MakeKargs FAST_EXP2 fold).
+        // Raw scores in place; the soft-cap variant turns them into r (see
+        // softcap_r_n: log2-unit score c (1 - 2 r), masked keys +inf), the
+        // others keep them, with scale*log2(e) folded into the exponent's FMA
+        // (CK MakeKargs FAST_EXP2 fold).
         float* s = reinterpret_cast<float*>(sr);
-        float a_coef = p.scale_log2;
         const int j0 = (it.jb + it.ub[t] + j) * C::BN;  // first key of this K/V tile
         if constexpr (XF == kXfSoftcap) {
-          tanh_n<W>(s, p.scale * p.softcap_inv);
-          a_coef = p.softcap * kLog2e;
+          softcap_r_n<W>(s, p.scale * p.softcap_inv);
         } else if constexpr (XF == kXfAlibi) {
           // CK ALiBi position encoding (slope per (batch, head), aligned like
           // the mask): natural-log score - slope*|diag - j|, in raw-score
@@ -890,15 +912,28 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           int hi = it.Lk - 1 - j0, lo = 0;  // kept columns [lo, hi] of this row
           if (MASK && p.win_right >= 0) hi = min(hi, qi + diag + p.win_right - j0);
           if (MASK && p.win_left >= 0) lo = qi + diag - p.win_left - j0;
+          constexpr float kDrop = XF == kXfSoftcap ? INFINITY : -INFINITY;  // a masked key
           if (lo <= 0) {  // no left bound inside the columns (plain causal or the tail)
 #pragma unroll
-            for (int c = 0; c < W; ++c) s[c] = c <= hi ? s[c] : -INFINITY;
+            for (int c = 0; c < W; ++c) s[c] = c <= hi ? s[c] : kDrop;
           } else {
 #pragma unroll
-            for (int c = 0; c < W; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : -INFINITY;
+            for (int c = 0; c < W; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : kDrop;
           }
         }
-        const float m_new = fmaxf(m_use, max_n<W>(s) * a_coef);  // a_coef > 0: order kept
+        // Row maximum in log2 units, and the exponent p = 2^(s a + b - msub).
+        float a_coef, b_coef, m_cand;
+        if constexpr (XF == kXfSoftcap) {
+          const float c2 = p.softcap * kLog2e;
+          a_coef = -2.0f * c2;
+          b_coef = c2;
+          m_cand = fmaf(min_n<W>(s), a_coef, c2);  // c (1 - 2 min r); -inf if all masked
+        } else {
+          a_coef = p.scale_log2;
+          b_coef = 0.0f;
+          m_cand = max_n<W>(s) * a_coef;  // a_coef > 0: order kept
+        }
+        const float m_new = fmaxf(m_use, m_cand);
         float alpha = 1.0f;
         if (m_new - m_use > 8.0f) {  // false when both are -inf (NaN compare)
           alpha = ex2_approx(m_use - m_new);
@@ -907,7 +942,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         const float msub = (m_use == -INFINITY) ? 0.0f : m_use;
         uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f in both lanes
         uint32_t pk[W / 2];
-        exp_pack_row<BF16, W / 2>(s, f2_pack(a_coef, a_coef), f2_pack(-msub, -msub), pk, acc2);
+        exp_pack_row<BF16, W / 2>(s, f2_pack(a_coef, a_coef),
+                                  f2_pack(b_coef - msub, b_coef - msub), pk, acc2);
         float r0, r1;
         f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), r0, r1);
         l = l * alpha + (r0 + r1);

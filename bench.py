@@ -336,13 +336,19 @@ def run_ours(args, rank, world, local):
                    "passes_per_step": passes, "ms_per_pass": round(ms_pass, 4),
                    "parallelism": f"independent batch per GPU x{world}",
                    "l2": "256 MiB buffer written before every pass (flush), outside the events"},
+        # The headline kernel runs back to back for the seconds-long timed loop
+        # (the GPU reaches its power cap), so its peak is the sustained bf16
+        # figure; the burst one is given beside it.
         "roofline": {"bound": "tensor", "achieved": round(kern_tflops, 2),
-                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(kern_tflops / pk["bf16_tflops"], 4),
+                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": round(kern_tflops / pk["bf16_tflops_sustained"], 4),
+                     "frac_of_burst_peak": round(kern_tflops / pk["bf16_tflops"], 4),
+                     "burst_peak": pk["bf16_tflops"],
                      "traffic": traffic_for("prefill_gqa_B2Hq32Hkv8L8192d128_causal",
                                             "prefill_kernel.cuh"),
-                     "peak_source": f"{pk_src} bf16 burst (MEASURED_PEAKS.json)"
-                     if pk_src == "measured" else "fallback 1.9 PFLOP/s",
+                     "peak_source": f"{pk_src} bf16 sustained (MEASURED_PEAKS.json), "
+                                    "a 3 s loop at the power cap"
+                     if pk_src == "measured" else "fallback 1.7 PFLOP/s sustained",
                      "kernel": kernel,
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": round(e2e_flops / (e2e_ms_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",

@@ -108,3 +108,22 @@ def test_varlen_parity(case):
                                 None if inp.sink is None else f64(inp.sink))
     check(o, lse, ro, rl, "varlen")
     no_device_error()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_softcap_logits_far_past_the_cap(d):
+    """Soft-cap 30 with rows 200-259 scaled so their logits run far past the
+    cap (Q x 40: tanh saturates, the kernel's r = 1 / (2^(2y log2 e) + 1)
+    reaches 0 and 1) next to rows with small logits, in one launch; every
+    row must match the oracle."""
+    inp = inputs.dense(1, 4, 2, 700, 700, d, "bf16", seed=70 + d, causal=True, softcap=30.0,
+                       with_sink=True)
+    q = inp.q.clone()
+    q[:, :, 200:260] = (q[:, :, 200:260].float() * 40.0).to(q.dtype)
+    o, lse = A.attn_fwd(cuda(q), cuda(inp.k), cuda(inp.v), causal=True, softcap=30.0,
+                        sink=cuda(inp.sink))
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn_dense(f64(q), f64(inp.k), f64(inp.v), 1 / math.sqrt(d), True, 30.0,
+                               f64(inp.sink))
+    check(o, lse, ro, rl, f"soft-cap far past the cap d={d}")
+    no_device_error()
