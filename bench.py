@@ -237,6 +237,66 @@ def time_steps(fn, steps, warmup, stream, flush, passes=1):
     return [sum(a.elapsed_time(b) for a, b in step) for step in evs]
 
 
+def e2e_pipelined(A, inp, steps, warmup):
+    """End-to-end steps of the headline workload through attn_fwd: per step,
+    Q, K, V from pinned host memory to the device, the attention, O and LSE
+    back to pinned host memory.  Three streams (host-to-device, compute,
+    device-to-host) and two device buffer sets; events order step k's
+    compute after its inputs arrive and its read-back after its compute, and
+    a buffer set is refilled only after the compute that used it.  Returns
+    (ms per step from the first input copy to the last read-back, bytes in
+    and out per step)."""
+    import torch
+    host = [t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v)]
+    B, Hq, L, _ = inp.q.shape
+    h_o = torch.empty(inp.q.shape, dtype=inp.q.dtype).pin_memory()
+    h_l = torch.empty((B, Hq, L), dtype=torch.float32).pin_memory()
+    dev = [[torch.empty_like(t) for t in (inp.q, inp.k, inp.v)] for _ in range(2)]
+    outs = [(torch.empty_like(inp.q), torch.empty((B, Hq, L), dtype=torch.float32, device="cuda"))
+            for _ in range(2)]
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(n):
+        arrived = [torch.cuda.Event() for _ in range(n)]
+        computed = [torch.cuda.Event() for _ in range(n)]
+        read = [torch.cuda.Event() for _ in range(n)]
+        for k in range(n):
+            b = k & 1
+            with torch.cuda.stream(s_in):
+                if k >= 2:
+                    s_in.wait_event(computed[k - 2])  # buffer set b is free again
+                for d, h in zip(dev[b], host):
+                    d.copy_(h, non_blocking=True)
+                arrived[k].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(arrived[k])
+                if k >= 2:
+                    s_comp.wait_event(read[k - 2])  # outputs b have been read back
+                q, kk, v = dev[b]
+                A.attn_fwd(q, kk, v, o=outs[b][0], lse=outs[b][1], causal=True, stream=s_comp)
+                computed[k].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[k])
+                h_o.copy_(outs[b][0], non_blocking=True)
+                h_l.copy_(outs[b][1], non_blocking=True)
+                read[k].record(s_out)
+        return read
+
+    run(warmup)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    read = run(steps)
+    end = torch.cuda.Event(enable_timing=True)
+    s_out.wait_event(read[-1])
+    end.record(s_out)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = h_o.numel() * h_o.element_size() + h_l.numel() * h_l.element_size()
+    return ms, h2d, d2h
+
+
 def make_flush():
     import torch
     buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
@@ -296,27 +356,13 @@ def run_ours(args, rank, world, local):
     kern_tflops = flops / (ms_pass * 1e-3) / 1e12
 
     # ---- e2e through the public API with host buffers ------------------------
-    hq = inp.q.cpu().pin_memory()
-    hk = inp.k.cpu().pin_memory()
-    hv = inp.v.cpu().pin_memory()
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(inp.q), torch.empty_like(inp.k), torch.empty_like(inp.v)
-
-    def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        A.attn_fwd(dq, dk, dv, o=o, lse=lse, causal=True)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-
-    e2e_times = time_steps(e2e_step, max(3, args.steps // 2), 2, stream, flush)
-    e2e_ms = statistics.mean(e2e_times)
+    # Every step copies its Q, K, V from pinned host memory and its O and LSE
+    # back.  The copies run on their own streams and overlap the neighbouring
+    # steps' attention (double-buffered device inputs and outputs): step k's
+    # inputs travel while step k-1 computes, its outputs while step k+1 does.
+    e2e_steps = max(3, args.steps // 2)
+    e2e_ms, h2d, d2h = e2e_pipelined(A, inp, e2e_steps, 2)
     e2e_flops, e2e_ms_max = aggregate(flops, e2e_ms, world)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-    del hq, hk, hv, ho, hl, dq, dk, dv
 
     result = {
         "metric": "attn fwd TFLOPS (causal prefill, unmasked pairs) & % of GB300 bf16 tensor peak",
@@ -353,7 +399,10 @@ def run_ours(args, rank, world, local):
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": round(e2e_flops / (e2e_ms_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms_max, 4)},
+                "ms_per_step": round(e2e_ms_max, 4), "steps": e2e_steps,
+                "pipeline": "copies on their own streams, overlapping the neighbouring steps' "
+                            "attention (double-buffered device tensors); every step's inputs "
+                            "go in and its outputs come out inside the timed region"},
         "gpu_launches": args.steps * passes,
         "clocks": clocks,
         "wall_s_timed_loop": round(wall, 3),
