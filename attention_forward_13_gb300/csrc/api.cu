@@ -83,12 +83,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Tiled map over a tensor whose innermost dimension is d (contiguous) and
-// whose other dimensions have the given extents and byte strides; the box is
-// 64 elements (128 bytes, one swizzle atom) by box[1..].
-// dt: attn_dtype of the elements (e4m3 travels as bytes).
+// Tiled map over a tensor whose innermost dimension is contiguous and whose
+// other dimensions have the given extents and byte strides, with the given
+// box.  dt: attn_dtype of the elements (e4m3 travels as bytes), or kMapF32.
+// Loads of Q/K/V use the 128-byte swizzle (one swizzle atom of 64 16-bit
+// elements per box row); the O store the 64-byte one; LSE none.
+constexpr int kMapF32 = -1;
 bool make_map(CUtensorMap* m, const void* base, int dt, int rank, const uint64_t* dims,
-              const uint64_t* strides_bytes, const uint32_t* box) {
+              const uint64_t* strides_bytes, const uint32_t* box,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   memset(m, 0, sizeof(*m));
@@ -101,13 +104,13 @@ bool make_map(CUtensorMap* m, const void* base, int dt, int rank, const uint64_t
     es[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
-  const CUtensorMapDataType ty = dt == ATTN_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                 : dt == ATTN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                  : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType ty = dt == kMapF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dt == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dt == ATTN_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUresult r = fn(m, ty,
                   rank, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -531,6 +534,23 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.lse_head = Lq;
   p.lse_batch = static_cast<int64_t>(Hq) * Lq;
   p.cu_q = p.cu_k = nullptr;
+  // TMA store of O and LSE (FlashAttention-3 epilogue store, the non-varlen
+  // path): each softmax warp owns 32 consecutive queries of one head when at
+  // most 4 heads share a tile.  LSE by TMA needs a 16-byte aligned base and
+  // rows of a multiple of 4 floats; otherwise each thread stores its own.
+  if (p.pack <= 4) {
+    const uint32_t obox[4] = {(uint32_t)(64 / eb), 32, 1, 1};
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lq, (uint64_t)Hq, (uint64_t)B};
+    const uint64_t st[3] = {(uint64_t)so.row * eb, (uint64_t)so.head * eb, (uint64_t)so.batch * eb};
+    p.o_tma = make_map(&p.tm_o, o, dtype, 4, dims, st, obox, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
+    if (lse != nullptr && aligned16(lse) && Lq % 4 == 0) {
+      const uint32_t lbox[3] = {32, 1, 1};
+      const uint64_t ldims[3] = {(uint64_t)Lq, (uint64_t)Hq, (uint64_t)B};
+      const uint64_t lst[2] = {(uint64_t)Lq * 4, (uint64_t)Hq * Lq * 4};
+      p.lse_tma =
+          make_map(&p.tm_lse, lse, kMapF32, 3, ldims, lst, lbox, CU_TENSOR_MAP_SWIZZLE_NONE) ? 1 : 0;
+    }
+  }
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

@@ -43,7 +43,7 @@ enum ScoreXf : int { kXfNone = 0, kXfSoftcap = 1, kXfAlibi = 2, kXfBias = 3 };
 // Bounds of the host-packed static schedule carried in PrefillParams, chosen
 // so that the launch parameters stay within 4 KB.
 constexpr int kSchedMaxCtas = 160;
-constexpr int kSchedMaxItems = 1536;
+constexpr int kSchedMaxItems = 1408;
 
 // Prefill (dense / varlen) launch parameters.  Tensor maps are 4-D
 // (d, rows, heads, batch); varlen problems use one batch slot and a row base.
@@ -51,6 +51,15 @@ struct PrefillParams {
   CUtensorMap tm_q;
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  // Dense problems whose softmax warps each own 32 consecutive queries of one
+  // head (no packing, or at most 4 heads per tile): the epilogue stores O and
+  // LSE by TMA through these maps (o_tma / lse_tma nonzero).  O: 4-D
+  // (d, Lq, Hq, B), box {64 bytes of d, 32 rows, 1, 1}, 64-byte swizzle; LSE:
+  // 3-D (Lq, Hq, B) fp32, box {32, 1, 1}.  Rows past Lq fall outside the
+  // maps and are not written.
+  CUtensorMap tm_o;
+  CUtensorMap tm_lse;
+  int o_tma, lse_tma;
   void* o;
   float* lse;
   int64_t o_row, o_head, o_batch;  // element strides of O

@@ -118,7 +118,10 @@ struct PrefillSmem : PrefillSmemFp8<C> {
   int abort_flag;
   // Epilogue staging, one 32-row x 64-byte block per softmax warp: rows go
   // in from the thread that owns them and out as 64-byte row pieces.
-  alignas(128) uint4 ostage[C::SOFT_WARPS][32 * 4];
+  // (1024-byte aligned: the TMA store reads it with the 64-byte swizzle, whose
+  // pattern repeats every 512 bytes.)
+  alignas(1024) uint4 ostage[C::SOFT_WARPS][32 * 4];
+  alignas(16) float lstage[C::SOFT_WARPS][32];  // LSE of the warp's rows (TMA store)
   // Group-mode / paged work order (order_items): slots heaviest first, each
   // slot's cost while sorting, per-cost bucket cursors, slots in use.
   uint16_t slot_order[kMaxSlots];
@@ -1006,8 +1009,23 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         oscale = (l > 0.0f) ? 1.0f / l : 0.0f;
       }
       const float lse_out = (ltot > 0.0f) ? (mfin + __log2f(ltot)) * kLn2 : -INFINITY;  // natural log
-      if (row_ok && p.lse != nullptr)
+      // The warp's 32 rows are 32 consecutive queries of one head when the
+      // stores go by TMA (host: at most 4 heads per tile): its first one and
+      // its head are the box's coordinates.
+      const int wq0 = mt + (((warp & 3) * 32) & qmask);
+      const int wh = it.h + (((warp & 3) * 32) >> p.qpt_log2);
+      if (p.lse_tma) {
+        // Rows past Lq fall outside the map: whatever they hold is not written.
+        sm.lstage[warp][lane] = lse_out;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && wq0 < it.Lq) {  // (a warp with no row inside issues nothing)
+          tma_store_3d(&p.tm_lse, sm.lstage[warp], wq0, wh, it.b);
+          bulk_commit();
+        }
+      } else if (row_ok && p.lse != nullptr) {
         p.lse[it.b * p.lse_batch + hr * p.lse_head + it.rq0 + qi] = lse_out;
+      }
       constexpr int OB = FP8 ? 1 : 2;  // bytes per output element
       // Output row of tile row R (its head and query; valid while the query
       // is inside the sequence).
@@ -1022,10 +1040,12 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         // O is read from tensor memory first (one wait) and goes back to the
         // MMA warp before any packing or store; then 64 bytes of each row
         // per round (32 fp16/bf16 or 64 e4m3 columns): each thread packs its
-        // row into the stage (16-byte pieces, XOR-swizzled by row pair so 8
-        // consecutive rows hit distinct banks), then the warp writes 8 rows
-        // x 64 contiguous bytes per instruction instead of 32 scattered
-        // 16-byte pieces.
+        // row into the stage (16-byte pieces, XOR-swizzled by row pair: the
+        // 64-byte swizzle, so 8 consecutive rows hit distinct banks).  Dense
+        // problems then store the stage with one TMA store per round (the
+        // FlashAttention-3 epilogue's non-varlen path); the others write 8
+        // rows x 64 contiguous bytes per instruction, row by row predicated
+        // (a box cannot stop at a packed sequence's end).
         constexpr int RC = 64 / OB;  // columns per round
         uint4* stage = sm.ostage[warp];
         const int lr = lane;
@@ -1039,8 +1059,13 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         reg_fence(ov);
         tc_fence_before();
         mbar_arrive(&sm.o_free[t]);
+        const bool tma = p.o_tma != 0;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += RC) {
+          if (tma && c0 > 0) {  // the previous round's store has read the stage
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
+          }
           if constexpr (FP8) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {  // 16 e4m3 columns per 16-byte piece
@@ -1066,6 +1091,15 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
               stage[lr * 4 + (q ^ ((lr >> 1) & 3))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
           }
+          if (tma) {
+            fence_proxy_async_smem();  // the stage, written here, is read by the async proxy
+            __syncwarp();
+            if (lane == 0 && wq0 < it.Lq) {
+              tma_store_4d(&p.tm_o, stage, c0, wq0, wh, it.b);
+              bulk_commit();
+            }
+            continue;
+          }
           __syncwarp();
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -1087,7 +1121,15 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < D * OB / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
       }
+      // Before the next item writes the stages again, this item's stores
+      // must have read them.
+      if (p.o_tma || p.lse_tma) {
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+      }
     }
+    // Every tensor store this warp issued has completed before the CTA ends.
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();

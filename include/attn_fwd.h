@@ -260,7 +260,7 @@ int attn_paged_window_pages(int Lq, int page_size, int max_pages_per_seq, const 
  * returns ATTN_OK for that grid.
  *   off: host int32 [grid + 1]; item: host int32 [B * U * ceil(Lq / Q)].
  *   Returns ATTN_ERR_UNSUPPORTED when the problem keeps the plain snake
- *   order (no mask, more than 1536 items or 160 CTAs, or no more items than
+ *   order (no mask, more than 1408 items or 160 CTAs, or no more items than
  *   CTAs), ATTN_ERR_INVALID for non-positive sizes, Hq % Hkv != 0 or NULL
  *   buffers.  Host only: needs no device.  opts as for attn_fwd (only the
  *   mask fields are read); may be NULL. */

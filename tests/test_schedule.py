@@ -123,7 +123,8 @@ def test_schedule_balances_the_headline_shape():
     ((4, 16, 2048, 2048, GRID), {}),                                  # no mask: plain order
     ((4, 16, 2048, 2048, GRID), {"window": (-1, -1)}),                # a window that keeps all
     ((1, 2, 2048, 2048, GRID), {"causal": True}),                     # 16 items <= 152 CTAs
-    ((16, 16, 2048, 2048, GRID), {"causal": True}),                   # 2048 items > 1536
+    ((16, 16, 2048, 2048, GRID), {"causal": True}),                   # 2048 items > 1408
+    ((11, 16, 2176, 2176, GRID), {"causal": True}),                   # 1584 items > 1408
     ((4, 16, 2048, 2048, 200), {"causal": True}),                     # grid > 160
 ])
 def test_schedule_not_used(args, kw):
@@ -141,3 +142,10 @@ def test_schedule_query_block_count_does_not_overflow():
     """Lq near 2^31: the block count is taken in 64 bits, so the problem is
     simply too large for the static schedule (no wrapped-around count)."""
     assert A.attn_dense_schedule(1, 1, 2 ** 31 - 10, 100, GRID, causal=True) is None
+
+
+def test_schedule_item_bound_is_inclusive():
+    """11 x 16 heads x 8 query blocks = 1408 items: the most the launch
+    parameters carry, scheduled."""
+    assert A.attn_dense_schedule(11, 16, 2048, 2048, GRID, causal=True) is not None
+
