@@ -1,7 +1,8 @@
 """A seeded random sweep of the three entry points against the fp64 oracle.
 
 Each case draws its shape and options at random within what the entry point
-accepts: batch, query and kv heads (GQA group 1-4), lengths (0 to a few
+accepts: batch, query and kv heads (GQA group 1-16, so every PackGQA factor
+and both epilogue store paths are drawn), lengths (0 to a few
 hundred, ragged, Lq != Lk), head dimension 64/128, fp16/bf16, causal, sliding
 window in either alignment, soft-cap, sink and ALiBi (the score transforms
 exclusive of one another), page size and split count for the paged cache.
@@ -50,7 +51,7 @@ def _dense_cases(n):
     for _ in range(n):
         B = int(rng.integers(1, 3))
         Hkv = int(rng.choice([1, 2, 4]))
-        g = int(rng.choice([1, 2, 4]))
+        g = int(rng.choice([1, 2, 4, 8, 16]))
         Lq = int(rng.integers(1, 513))
         Lk = Lq if rng.random() < 0.5 else int(rng.integers(1, 513))
         d = int(rng.choice([64, 128]))
@@ -67,7 +68,7 @@ def _varlen_cases(n):
         lq = [int(x) for x in rng.integers(0, 400, B)]
         lk = lq if rng.random() < 0.5 else [int(x) for x in rng.integers(0, 400, B)]
         Hkv = int(rng.choice([1, 2]))
-        g = int(rng.choice([1, 2, 4]))
+        g = int(rng.choice([1, 2, 4, 8, 16]))
         d = int(rng.choice([64, 128]))
         dt = str(rng.choice(["bf16", "f16"]))
         out.append((lq, lk, Hkv * g, Hkv, d, dt) + _options(rng) + (int(rng.integers(1 << 30)),))
