@@ -1020,7 +1020,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && wq0 < it.Lq) {  // (a warp with no row inside issues nothing)
-          tma_store_3d(&p.tm_lse, sm.lstage[warp], wq0, wh, it.b);
+          if constexpr (ATTN_L2_HINTS)
+            tma_store_3d_hint(&p.tm_lse, sm.lstage[warp], wq0, wh, it.b, l2_policy_evict_first());
+          else
+            tma_store_3d(&p.tm_lse, sm.lstage[warp], wq0, wh, it.b);
           bulk_commit();
         }
       } else if (row_ok && p.lse != nullptr) {
@@ -1095,7 +1098,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
             fence_proxy_async_smem();  // the stage, written here, is read by the async proxy
             __syncwarp();
             if (lane == 0 && wq0 < it.Lq) {
-              tma_store_4d(&p.tm_o, stage, c0, wq0, wh, it.b);
+              if constexpr (ATTN_L2_HINTS) tma_store_4d_hint(&p.tm_o, stage, c0, wq0, wh, it.b, pol_o);
+              else tma_store_4d(&p.tm_o, stage, c0, wq0, wh, it.b);
               bulk_commit();
             }
             continue;
