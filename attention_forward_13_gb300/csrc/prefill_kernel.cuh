@@ -13,8 +13,10 @@
 // GQA kv head = h / ratio, heaviest causal tiles first, the scale*log2(e)
 // fold).  The Blackwell design here differs from all three:
 //
-//  * persistent: one CTA per SM walks a list of work items (a 256-row query
-//    block of one (batch, head)): dense masked problems run the per-CTA
+//  * persistent: one CTA per SM walks a list of work items (a query block of
+//    two 128-row tiles of one batch and one head group; with PackGQA a tile
+//    holds 128 / g queries of each of the g query heads of a kv head, which
+//    then share every K/V tile in shared memory): dense masked problems run the per-CTA
 //    lists the host packed for the shape (longest processing time first),
 //    other dense problems a snake order across CTAs; in group mode and over
 //    a paged cache every CTA first sorts the (query block, sequence) pairs
@@ -32,6 +34,9 @@
 //    subtrahend is only raised when the row max grows by more than 8 (log2
 //    units); otherwise O is not rescaled.  This is exact: the final O/l and
 //    LSE use the same subtrahend.
+//  * the epilogue stages each warp's rows in shared memory (64-byte swizzle)
+//    and stores them with TMA for dense problems, row by row with predicates
+//    in group mode and over a paged cache.
 //  * every mbarrier wait is bounded (Waiter): a CTA that gives up records a
 //    bit in the device error word, drains its own copies and MMAs, frees its
 //    tensor memory and returns.
