@@ -539,10 +539,12 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   // most 4 heads share a tile.  LSE by TMA needs a 16-byte aligned base and
   // rows of a multiple of 4 floats; otherwise each thread stores its own.
   if (p.pack <= 4) {
-    const uint32_t obox[4] = {(uint32_t)(64 / eb), 32, 1, 1};
+    const int rb = prefill_o_round_bytes(dt == kDtE4M3, p.pack);  // bytes per row and store
+    const uint32_t obox[4] = {(uint32_t)(rb / eb), 32, 1, 1};
     const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Lq, (uint64_t)Hq, (uint64_t)B};
     const uint64_t st[3] = {(uint64_t)so.row * eb, (uint64_t)so.head * eb, (uint64_t)so.batch * eb};
-    p.o_tma = make_map(&p.tm_o, o, dtype, 4, dims, st, obox, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
+    p.o_tma = make_map(&p.tm_o, o, dtype, 4, dims, st, obox,
+                       rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ? rb : 0;
     if (lse != nullptr && aligned16(lse) && Lq % 4 == 0) {
       const uint32_t lbox[3] = {32, 1, 1};
       const uint64_t ldims[3] = {(uint64_t)Lq, (uint64_t)Hq, (uint64_t)B};

@@ -7,7 +7,19 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+// Bytes of each output row the dense prefill epilogue stages and stores per
+// round (one TMA store per softmax warp and round): 128 without PackGQA, 64
+// with packed heads (measured) and for FP8 (whose widened V buffers take the
+// shared memory a 128-byte stage would need).
+#ifndef ATTN_O_ROUND_BYTES
+#define ATTN_O_ROUND_BYTES 128
+#endif
+
 namespace attn {
+
+constexpr int prefill_o_round_bytes(bool fp8, int pack) {
+  return (fp8 || pack > 1) ? 64 : ATTN_O_ROUND_BYTES;
+}
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -54,12 +66,12 @@ struct PrefillParams {
   // Dense problems whose softmax warps each own 32 consecutive queries of one
   // head (no packing, or at most 4 heads per tile): the epilogue stores O and
   // LSE by TMA through these maps (o_tma / lse_tma nonzero).  O: 4-D
-  // (d, Lq, Hq, B), box {64 bytes of d, 32 rows, 1, 1}, 64-byte swizzle; LSE:
-  // 3-D (Lq, Hq, B) fp32, box {32, 1, 1}.  Rows past Lq fall outside the
-  // maps and are not written.
+  // (d, Lq, Hq, B), box {o_tma bytes of d (64 or 128), 32 rows, 1, 1},
+  // swizzle of the same width; LSE: 3-D (Lq, Hq, B) fp32, box {32, 1, 1}.
+  // Rows past Lq fall outside the maps and are not written.
   CUtensorMap tm_o;
   CUtensorMap tm_lse;
-  int o_tma, lse_tma;
+  int o_tma, lse_tma;  // o_tma: bytes of each row per store (0: no map)
   void* o;
   float* lse;
   int64_t o_row, o_head, o_batch;  // element strides of O

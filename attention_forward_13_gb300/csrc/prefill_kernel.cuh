@@ -56,6 +56,12 @@
 #define ATTN_L2_HINTS 1
 #endif
 
+// P handed to the MMA warp in two halves of 64 keys: the P.V MMAs of the
+// first half start while the softmax computes the second.
+#ifndef ATTN_P_HALVES
+#define ATTN_P_HALVES 1
+#endif
+
 namespace attn {
 
 template <int D_, int DT_ = kDtBF16>
@@ -110,29 +116,42 @@ struct PrefillSmemFp8<C, true> {
   uint64_t vc_full[C::NVC], vc_empty[C::NVC];
 };
 
-template <class C>
-struct PrefillSmem : PrefillSmemFp8<C> {
+// Group-mode / paged work order (order_items): slots heaviest first, each
+// slot's cost while sorting, per-cost bucket cursors, slots in use.  Dense
+// kernels take their order from the host and carry none of it.
+template <bool ORD>
+struct PrefillSmemOrder {};
+template <>
+struct PrefillSmemOrder<true> {
+  uint16_t slot_order[kMaxSlots];
+  uint8_t slot_cost[kMaxSlots];
+  int cost_cursor[256];
+  int n_slots;
+};
+
+// Bytes of each output row staged per epilogue round: dense problems store
+// whole rounds by TMA; group mode and paged caches write row pieces from a
+// smaller stage.
+template <class C, bool ORD>
+constexpr int kStageRowBytes = ORD ? 64 : prefill_o_round_bytes(C::FP8, 1);
+
+template <class C, bool ORD>
+struct PrefillSmem : PrefillSmemFp8<C>, PrefillSmemOrder<ORD> {
   alignas(1024) uint8_t q[2][C::TILE_BYTES];
   alignas(1024) uint8_t k[C::NS][C::TILE_BYTES];
   alignas(1024) uint8_t v[C::NS][C::TILE_BYTES];
   uint64_t q_full[2], q_empty[2];  // per query tile
   uint64_t k_full[C::NS], k_empty[C::NS], v_full[C::NS], v_empty[C::NS];
-  uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
+  uint64_t s_full[2], p_half[2], p_full[2], o_final[2], o_free[2];
   uint64_t teardown;
   uint32_t tmem_base;
   int abort_flag;
-  // Epilogue staging, one 32-row x 64-byte block per softmax warp: rows go
-  // in from the thread that owns them and out as 64-byte row pieces.
-  // (1024-byte aligned: the TMA store reads it with the 64-byte swizzle, whose
-  // pattern repeats every 512 bytes.)
-  alignas(1024) uint4 ostage[C::SOFT_WARPS][32 * 4];
+  // Epilogue staging, one 32-row block per softmax warp (kStageRowBytes per
+  // row): rows go in from the thread that owns them and out by TMA or as
+  // row pieces.  (1024-byte aligned: the TMA store reads it with the 64- or
+  // 128-byte swizzle, whose pattern repeats every 512 or 1024 bytes.)
+  alignas(1024) uint4 ostage[C::SOFT_WARPS][32 * kStageRowBytes<C, ORD> / 16];
   alignas(16) float lstage[C::SOFT_WARPS][32];  // LSE of the warp's rows (TMA store)
-  // Group-mode / paged work order (order_items): slots heaviest first, each
-  // slot's cost while sorting, per-cost bucket cursors, slots in use.
-  uint16_t slot_order[kMaxSlots];
-  uint8_t slot_cost[kMaxSlots];
-  int cost_cursor[256];
-  int n_slots;
 };
 
 // Maximum of N values: a tree of 3-input max instructions (N = 128: 64
@@ -444,7 +463,7 @@ __device__ __forceinline__ bool decode_item(const PrefillParams& p, const ItemOr
 // first, and one warp places the slots in slot order within a cost, so that
 // every CTA builds the same list.
 template <int BM, int BN, bool MASK, class C>
-__device__ void order_items(const PrefillParams& p, PrefillSmem<C>& sm) {
+__device__ void order_items(const PrefillParams& p, PrefillSmem<C, true>& sm) {
   const int nslots = p.num_m_blocks * p.B;
   if ((p.cu_q == nullptr && p.seqlens_k == nullptr) || nslots > kMaxSlots) {
     if (threadIdx.x == 0) sm.n_slots = -1;
@@ -517,8 +536,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
   using C = PrefillCfg<D, DT>;
   constexpr bool FP8 = C::FP8;
   constexpr bool BF16 = DT == kDtBF16;  // P / V type of the P.V MMA (FP8: fp16)
+  // P in two halves where the score transform leaves the registers for it
+  // (ALiBi and the elementwise bias would spill).
+  constexpr bool HALVES = ATTN_P_HALVES && (XF == kXfNone || XF == kXfSoftcap);
   extern __shared__ uint8_t smem_raw[];
-  PrefillSmem<C>& sm = *reinterpret_cast<PrefillSmem<C>*>(
+  PrefillSmem<C, ORD>& sm = *reinterpret_cast<PrefillSmem<C, ORD>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5;
@@ -543,7 +565,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
-      mbar_init(&sm.p_full[t], 128);  // every softmax thread of the tile
+      mbar_init(&sm.p_half[t], 128);  // every softmax thread of the tile
+      mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_final[t], 1);
       mbar_init(&sm.o_free[t], 128);
     }
@@ -686,12 +709,13 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         }
         umma_commit_warp(&sm.s_full[t], lead);
       };
-      auto issue_pv = [&](int t, int g, bool acc) {  // O_t (+)= P_t V_g
+      // O_t (+)= P_t V_g over keys [16 k0, 16 k1) of the tile.
+      auto issue_pv = [&](int t, int g, bool acc, int k0, int k1) {
         uint64_t vd;
         if constexpr (FP8) vd = sdesc_sw128(smem_u32(sm.vc[g % C::NVC]), C::CHUNK_BYTES, 1024);
         else vd = vdesc0 + static_cast<uint64_t>((g % C::NS) * kTileDesc);
 #pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k) {  // 16 keys per MMA
+        for (int k = k0; k < k1; ++k) {  // 16 keys per MMA
           umma_ts_warp(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8, vd + ((k * 16 * 128) >> 4),
                        idesc_o, (acc || k > 0) ? 1u : 0u, lead);
         }
@@ -736,14 +760,23 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (it.ub[t] <= u && u < it.ue[t]) {
-              if (!(ok = w.wait(&sm.p_full[t], pc[t] & 1, kErrPrefillPFull))) break;
-              ++pc[t];
+              if (!(ok = w.wait(HALVES ? &sm.p_half[t] : &sm.p_full[t], pc[t] & 1,
+                                kErrPrefillPFull)))
+                break;
               // O_t is free once the previous item's epilogue has read it.
               if (u == it.ub[t] && oc[t] > 0 &&
                   !(ok = w.wait(&sm.o_free[t], (oc[t] - 1) & 1, kErrPrefillOFinal)))
                 break;
               tc_fence_after();
-              issue_pv(t, gu, u > it.ub[t]);
+              if constexpr (HALVES) {
+                issue_pv(t, gu, u > it.ub[t], 0, C::BN / 32);
+                if (!(ok = w.wait(&sm.p_full[t], pc[t] & 1, kErrPrefillPFull))) break;
+                tc_fence_after();
+                issue_pv(t, gu, true, C::BN / 32, C::BN / 16);
+              } else {
+                issue_pv(t, gu, u > it.ub[t], 0, C::BN / 16);
+              }
+              ++pc[t];
               if (u + 1 == it.ue[t]) umma_commit_warp(&sm.o_final[t], lead);
             }
             // No fence of its own: S_t(u+1) is ordered after this tile's
@@ -948,33 +981,48 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
           m_use = m_new;
         }
         const float msub = (m_use == -INFINITY) ? 0.0f : m_use;
+        // The P.V MMA of the previous K/V tile finished before this S was
+        // produced (its commit covers every earlier MMA), so O can be
+        // rescaled now; with P in halves, before the first half goes out.
+        auto rescale_o = [&]() {
+          if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+              uint32_t ov[32];
+              tmem_ld32(tO + c, ov);
+              tmem_ld_wait();
+              reg_fence(ov);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+              tmem_st32(tO + c, ov);
+            }
+          }
+        };
         uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f in both lanes
         uint32_t pk[W / 2];
-        exp_pack_row<BF16, W / 2>(s, f2_pack(a_coef, a_coef),
-                                  f2_pack(b_coef - msub, b_coef - msub), pk, acc2);
+        const uint64_t a2 = f2_pack(a_coef, a_coef), b2 = f2_pack(b_coef - msub, b_coef - msub);
+        if constexpr (HALVES) {
+          static_assert(W == 128, "P halves of one 32-column store each");
+          exp_pack_row<BF16, W / 4>(s, a2, b2, pk, acc2);
+          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          rescale_o();  // (here, with half of the scores consumed: fewer live registers)
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&sm.p_half[t]);
+          exp_pack_row<BF16, W / 4>(s + W / 2, a2, b2, pk + W / 4, acc2);
+          tmem_st32(tS + W / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk[W / 4]));
+        } else {
+          exp_pack_row<BF16, W / 2>(s, a2, b2, pk, acc2);
+          // P over the first W/2 columns of S.
+#pragma unroll
+          for (int qq = 0; qq < W / 64; ++qq)
+            tmem_st32(tS + 32 * qq, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * qq]));
+        }
         float r0, r1;
         f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), r0, r1);
         l = l * alpha + (r0 + r1);
-        // P over the first W/2 columns of S.
-#pragma unroll
-        for (int qq = 0; qq < W / 64; ++qq)
-          tmem_st32(tS + 32 * qq, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * qq]));
-        // The P.V MMA of the previous K/V tile finished before this S was
-        // produced (its commit covers every earlier MMA), so O can be
-        // rescaled now.
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t ov[32];
-            tmem_ld32(tO + c, ov);
-            tmem_ld_wait();
-            reg_fence(ov);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(tO + c, ov);
-          }
-        }
+        if constexpr (!HALVES) rescale_o();
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full[t]);
@@ -1019,6 +1067,12 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       // its head are the box's coordinates.
       const int wq0 = mt + (((warp & 3) * 32) & qmask);
       const int wh = it.h + (((warp & 3) * 32) >> p.qpt_log2);
+      // The previous item's stores have read the stages (they had this
+      // item's K/V steps to do it, so this rarely waits).
+      if (p.o_tma || p.lse_tma) {
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+      }
       if (p.lse_tma) {
         // Rows past Lq fall outside the map: whatever they hold is not written.
         sm.lstage[warp][lane] = lse_out;
@@ -1046,17 +1100,16 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
       };
       if (have_o) {
         // O is read from tensor memory first (one wait) and goes back to the
-        // MMA warp before any packing or store; then 64 bytes of each row
-        // per round (32 fp16/bf16 or 64 e4m3 columns): each thread packs its
-        // row into the stage (16-byte pieces, XOR-swizzled by row pair: the
-        // 64-byte swizzle, so 8 consecutive rows hit distinct banks).  Dense
-        // problems then store the stage with one TMA store per round (the
-        // FlashAttention-3 epilogue's non-varlen path); the others write 8
-        // rows x 64 contiguous bytes per instruction, row by row predicated
-        // (a box cannot stop at a packed sequence's end).
-        constexpr int RC = 64 / OB;  // columns per round
-        uint4* stage = sm.ostage[warp];
-        const int lr = lane;
+        // MMA warp before any packing or store; then RB bytes of each row per
+        // round: each thread packs its row into the stage (16-byte pieces,
+        // XOR-swizzled like the TMA store's 64- or 128-byte swizzle, so 8
+        // consecutive rows hit distinct banks).  Dense problems then store the
+        // stage with one TMA store per round (the FlashAttention-3 epilogue's
+        // non-varlen path); the others write 32 / (RB / 16) rows x RB bytes
+        // per instruction, row by row predicated (a box cannot stop at a
+        // packed sequence's end).  Rounds of 128 bytes where the host asks
+        // for them (problems without PackGQA: measured faster there, slower
+        // with packed heads), else 64.
         const uint64_t pol_o = l2_policy_evict_first();
         (void)pol_o;
         if constexpr (FP8) oscale *= p.o_scale;  // FP8 static quantisation: scale_p * scale_o
@@ -1068,60 +1121,75 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(&sm.o_free[t]);
         const bool tma = p.o_tma != 0;
+        uint4* stage = sm.ostage[warp];
+        auto rounds = [&](auto rb_c) {
+          constexpr int RB = decltype(rb_c)::value;  // bytes of each row per round
+          constexpr int RC = RB / OB;                // columns per round
+          constexpr int LPR = RB / 16;               // 16-byte pieces of a row per round
+          static_assert(RB == 64 || RB == 128, "64- or 128-byte rounds");
+          const int lr = lane;
+          auto sw = [](int R) { return ((R * RB) >> 7) & (LPR - 1); };  // piece q of row R at q ^ sw(R)
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += RC) {
-          if (tma && c0 > 0) {  // the previous round's store has read the stage
-            if (lane == 0) bulk_wait_read();
+          for (int c0 = 0; c0 < D; c0 += RC) {
+            if (tma && c0 > 0) {  // the previous round's store has read the stage
+              if (lane == 0) bulk_wait_read();
+              __syncwarp();
+            }
+            if constexpr (FP8) {
+#pragma unroll
+              for (int q = 0; q < LPR; ++q) {  // 16 e4m3 columns per 16-byte piece
+                uint32_t w4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const uint32_t* x = &ov[c0 + 16 * q + 4 * i];
+                  w4[i] = pack_e4m3x4(__uint_as_float(x[0]) * oscale, __uint_as_float(x[1]) * oscale,
+                                      __uint_as_float(x[2]) * oscale, __uint_as_float(x[3]) * oscale);
+                }
+                stage[lr * LPR + (q ^ sw(lr))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < LPR; ++q) {  // 8 fp16/bf16 columns per 16-byte piece
+                uint32_t w4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float a = __uint_as_float(ov[c0 + 8 * q + 2 * i]) * oscale;
+                  const float bb = __uint_as_float(ov[c0 + 8 * q + 2 * i + 1]) * oscale;
+                  w4[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
+                }
+                stage[lr * LPR + (q ^ sw(lr))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
+            }
+            if (tma) {
+              fence_proxy_async_smem();  // the stage, written here, is read by the async proxy
+              __syncwarp();
+              if (lane == 0) {
+                if constexpr (ATTN_L2_HINTS) tma_store_4d_hint(&p.tm_o, stage, c0, wq0, wh, it.b, pol_o);
+                else tma_store_4d(&p.tm_o, stage, c0, wq0, wh, it.b);
+                bulk_commit();
+              }
+              continue;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < LPR; ++k) {  // 32 / LPR rows per instruction
+              const int rw = (32 / LPR) * k + lr / LPR, q = lr % LPR;
+              const uint4 v4 = stage[rw * LPR + (q ^ sw(rw))];
+              bool valid;
+              uint8_t* dst = orow((warp & 3) * 32 + rw, valid);
+              if (valid) {
+                if constexpr (ATTN_L2_HINTS) st_global_v4_hint(dst + c0 * OB + 16 * q, v4, pol_o);
+                else *reinterpret_cast<uint4*>(dst + c0 * OB + 16 * q) = v4;
+              }
+            }
             __syncwarp();
           }
-          if constexpr (FP8) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {  // 16 e4m3 columns per 16-byte piece
-              uint32_t w4[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t* x = &ov[c0 + 16 * q + 4 * i];
-                w4[i] = pack_e4m3x4(__uint_as_float(x[0]) * oscale, __uint_as_float(x[1]) * oscale,
-                                    __uint_as_float(x[2]) * oscale, __uint_as_float(x[3]) * oscale);
-              }
-              stage[lr * 4 + (q ^ ((lr >> 1) & 3))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {  // 8 fp16/bf16 columns per 16-byte piece
-              uint32_t w4[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float a = __uint_as_float(ov[c0 + 8 * q + 2 * i]) * oscale;
-                const float bb = __uint_as_float(ov[c0 + 8 * q + 2 * i + 1]) * oscale;
-                w4[i] = BF16 ? pack_bf16(a, bb) : pack_f16(a, bb);
-              }
-              stage[lr * 4 + (q ^ ((lr >> 1) & 3))] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-          }
-          if (tma) {
-            fence_proxy_async_smem();  // the stage, written here, is read by the async proxy
-            __syncwarp();
-            if (lane == 0 && wq0 < it.Lq) {
-              if constexpr (ATTN_L2_HINTS) tma_store_4d_hint(&p.tm_o, stage, c0, wq0, wh, it.b, pol_o);
-              else tma_store_4d(&p.tm_o, stage, c0, wq0, wh, it.b);
-              bulk_commit();
-            }
-            continue;
-          }
-          __syncwarp();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int rw = 8 * k + (lr >> 2), q = lr & 3;
-            const uint4 v4 = stage[rw * 4 + (q ^ ((rw >> 1) & 3))];
-            bool valid;
-            uint8_t* dst = orow((warp & 3) * 32 + rw, valid);
-            if (valid) {
-              if constexpr (ATTN_L2_HINTS) st_global_v4_hint(dst + c0 * OB + 16 * q, v4, pol_o);
-              else *reinterpret_cast<uint4*>(dst + c0 * OB + 16 * q) = v4;
-            }
-          }
-          __syncwarp();
+        };
+        if constexpr (kStageRowBytes<C, ORD> == 128) {
+          if (p.o_tma == 64) rounds(std::integral_constant<int, 64>{});
+          else rounds(std::integral_constant<int, 128>{});
+        } else {
+          rounds(std::integral_constant<int, 64>{});
         }
       } else if (row_ok) {
         bool valid;  // == row_ok
@@ -1129,12 +1197,6 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         (void)valid;
 #pragma unroll
         for (int i = 0; i < D * OB / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-      }
-      // Before the next item writes the stages again, this item's stores
-      // must have read them.
-      if (p.o_tma || p.lse_tma) {
-        if (lane == 0) bulk_wait_read();
-        __syncwarp();
       }
     }
     // Every tensor store this warp issued has completed before the CTA ends.
@@ -1153,7 +1215,8 @@ template <int D, int DT, bool MASK, int XF, bool ORD = false>
 static cudaError_t launch_prefill_t(const PrefillParams& p, int grid, cudaStream_t stream) {
   using C = PrefillCfg<D, DT>;
   auto kern = attn_prefill_kernel<D, DT, MASK, XF, ORD>;
-  const int smem = static_cast<int>(sizeof(PrefillSmem<C>)) + 1024;
+  const int smem = static_cast<int>(sizeof(PrefillSmem<C, ORD>)) + 1024;
+  static_assert(sizeof(PrefillSmem<C, ORD>) + 1024 <= 227 * 1024, "shared memory per block");
   static bool configured = false;  // per instantiation; attribute set is idempotent
   if (!configured) {
     // The softmax warpgroups raise their register budget with setmaxnreg,
