@@ -29,14 +29,17 @@
 //    exponentials the tensor core works on the other tile (ping-pong).
 //  * S lives in tensor memory (fp32, 128 columns per tile).  The softmax
 //    writes P (bf16/fp16) back over the first 64 columns of its S and the
-//    P.V MMA reads its A operand straight from tensor memory.
+//    P.V MMA reads its A operand straight from tensor memory; P goes out in
+//    two halves of 64 keys, so the first half's P.V MMAs run while the
+//    second half is computed.
 //  * O accumulates in tensor memory.  The running max used as the exp2
 //    subtrahend is only raised when the row max grows by more than 8 (log2
 //    units); otherwise O is not rescaled.  This is exact: the final O/l and
 //    LSE use the same subtrahend.
-//  * the epilogue stages each warp's rows in shared memory (64-byte swizzle)
-//    and stores them with TMA for dense problems, row by row with predicates
-//    in group mode and over a paged cache.
+//  * the epilogue stages each warp's rows in shared memory (128 or 64 bytes
+//    of each row per round, swizzled like the TMA store) and stores them with
+//    TMA for dense problems, row by row with predicates in group mode and
+//    over a paged cache.
 //  * every mbarrier wait is bounded (Waiter): a CTA that gives up records a
 //    bit in the device error word, drains its own copies and MMAs, frees its
 //    tensor memory and returns.
