@@ -61,6 +61,11 @@
 
 // P handed to the MMA warp in two halves of 64 keys: the P.V MMAs of the
 // first half start while the softmax computes the second.
+// Row maxima taken by the tensor-memory load (tcgen05.ld.red.max, sm_103a)
+// where no key of the tile is masked, instead of a 3-input max tree.
+#ifndef ATTN_HW_ROW_MAX
+#define ATTN_HW_ROW_MAX 1
+#endif
 #ifndef ATTN_P_HALVES
 #define ATTN_P_HALVES 1
 #endif
@@ -542,6 +547,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
   // P in two halves where the score transform leaves the registers for it
   // (ALiBi and the elementwise bias would spill).
   constexpr bool HALVES = ATTN_P_HALVES && (XF == kXfNone || XF == kXfSoftcap);
+  // Row maxima from the tensor-memory load itself (sm_103a tcgen05.ld.red) on
+  // tiles without masked keys, for untransformed scores (with the soft-cap,
+  // measured slower: the scalar tanh of the maximum then sits on the chain
+  // and the kernel spills).
+  constexpr bool HW_MAX = ATTN_HW_ROW_MAX && XF == kXfNone;
   extern __shared__ uint8_t smem_raw[];
   PrefillSmem<C, ORD>& sm = *reinterpret_cast<PrefillSmem<C, ORD>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -894,6 +904,14 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         ++pc;
         tc_fence_after();
         uint32_t sr[W];
+        const int j0 = (it.jb + it.ub[t] + j) * C::BN;  // first key of this K/V tile
+        // Whether some key of this tile is masked for some row of the tile
+        // (the tail past Lk, the causal / window band): the same for every
+        // thread of the warpgroup.
+        const bool masked = (j0 + W > it.Lk) ||
+                            (MASK && p.win_right >= 0 && j0 + W - 1 > mt + diag + p.win_right) ||
+                            (MASK && p.win_left >= 0 && j0 < last + diag - p.win_left);
+        float raw_max = -INFINITY;  // (HW_MAX) the row maximum of the raw scores
         if constexpr (XF == kXfBias) {
           // A quarter of 32 scores at a time, each taking its bias from
           // registers as it lands, so that the prefetched segment and the
@@ -907,6 +925,20 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
             if (qi < it.Lq)
               add_bias_quarter<BF16>(reinterpret_cast<float*>(&sr[32 * qq]), &bn[4 * qq], p.inv_scale);
           }
+        } else if (HW_MAX) {
+          // The row maximum of the raw scores comes with the load (used where
+          // no key of the tile is masked and the transform keeps the order).
+          uint32_t m4[W / 32];
+#pragma unroll
+          for (int qq = 0; qq < W / 32; ++qq)
+            tmem_ld32_max(tS + 32 * qq, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * qq]),
+                          *reinterpret_cast<float*>(&m4[qq]));
+          tmem_ld_wait();
+          reg_fence(sr);
+          reg_fence(m4);
+          static_assert(W == 128, "four partial maxima");
+          raw_max = fmaxf(fmax3(__uint_as_float(m4[0]), __uint_as_float(m4[1]),
+                                __uint_as_float(m4[2])), __uint_as_float(m4[3]));
         } else {
 #pragma unroll
           for (int qq = 0; qq < W / 32; ++qq)
@@ -919,7 +951,6 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         // others keep them, with scale*log2(e) folded into the exponent's FMA
         // (CK MakeKargs FAST_EXP2 fold).
         float* s = reinterpret_cast<float*>(sr);
-        const int j0 = (it.jb + it.ub[t] + j) * C::BN;  // first key of this K/V tile
         if constexpr (XF == kXfSoftcap) {
           softcap_r_n<W>(s, p.scale * p.softcap_inv);
         } else if constexpr (XF == kXfAlibi) {
@@ -950,32 +981,43 @@ __global__ void __launch_bounds__(PrefillCfg<D, DT>::THREADS, 1)
         }
         // (The elementwise bias was added above, as the scores left tensor
         // memory.)
-        if ((j0 + W > it.Lk) ||
-            (MASK && p.win_right >= 0 && j0 + W - 1 > mt + diag + p.win_right) ||
-            (MASK && p.win_left >= 0 && j0 < last + diag - p.win_left)) {
-          int hi = it.Lk - 1 - j0, lo = 0;  // kept columns [lo, hi] of this row
-          if (MASK && p.win_right >= 0) hi = min(hi, qi + diag + p.win_right - j0);
-          if (MASK && p.win_left >= 0) lo = qi + diag - p.win_left - j0;
-          constexpr float kDrop = XF == kXfSoftcap ? INFINITY : -INFINITY;  // a masked key
-          if (lo <= 0) {  // no left bound inside the columns (plain causal or the tail)
-#pragma unroll
-            for (int c = 0; c < W; ++c) s[c] = c <= hi ? s[c] : kDrop;
-          } else {
-#pragma unroll
-            for (int c = 0; c < W; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : kDrop;
-          }
-        }
         // Row maximum in log2 units, and the exponent p = 2^(s a + b - msub).
         float a_coef, b_coef, m_cand;
         if constexpr (XF == kXfSoftcap) {
-          const float c2 = p.softcap * kLog2e;
-          a_coef = -2.0f * c2;
-          b_coef = c2;
-          m_cand = fmaf(min_n<W>(s), a_coef, c2);  // c (1 - 2 min r); -inf if all masked
+          a_coef = -2.0f * p.softcap * kLog2e;
+          b_coef = p.softcap * kLog2e;
         } else {
           a_coef = p.scale_log2;
           b_coef = 0.0f;
-          m_cand = max_n<W>(s) * a_coef;  // a_coef > 0: order kept
+        }
+        if (HW_MAX && !masked) {
+          if constexpr (XF == kXfSoftcap) {
+            // min r is r of the largest raw score (r decreases with the
+            // score), computed as softcap_r_n does for every score.
+            const float r_min =
+                rcp_approx(ex2_approx(raw_max * (p.scale * p.softcap_inv * 2.0f * kLog2e)) + 1.0f);
+            m_cand = fmaf(r_min, a_coef, b_coef);  // c (1 - 2 min r)
+          } else {
+            m_cand = raw_max * a_coef;  // a_coef > 0: order kept
+          }
+        } else {
+          if (masked) {
+            int hi = it.Lk - 1 - j0, lo = 0;  // kept columns [lo, hi] of this row
+            if (MASK && p.win_right >= 0) hi = min(hi, qi + diag + p.win_right - j0);
+            if (MASK && p.win_left >= 0) lo = qi + diag - p.win_left - j0;
+            constexpr float kDrop = XF == kXfSoftcap ? INFINITY : -INFINITY;  // a masked key
+            if (lo <= 0) {  // no left bound inside the columns (plain causal or the tail)
+#pragma unroll
+              for (int c = 0; c < W; ++c) s[c] = c <= hi ? s[c] : kDrop;
+            } else {
+#pragma unroll
+              for (int c = 0; c < W; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : kDrop;
+            }
+          }
+          if constexpr (XF == kXfSoftcap)
+            m_cand = fmaf(min_n<W>(s), a_coef, b_coef);  // c (1 - 2 min r); -inf if all masked
+          else
+            m_cand = max_n<W>(s) * a_coef;  // a_coef > 0: order kept
         }
         const float m_new = fmaxf(m_use, m_cand);
         float alpha = 1.0f;
