@@ -245,7 +245,8 @@ def e2e_pipelined(A, inp, steps, warmup):
     compute after its inputs arrive and its read-back after its compute, and
     a buffer set is refilled only after the compute that used it.  Returns
     (ms per step from the first input copy to the last read-back, bytes in
-    and out per step)."""
+    and out per step, ms per step of the same copies alone with both
+    directions at once: the host link's bound on a step)."""
     import torch
     host = [t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v)]
     B, Hq, L, _ = inp.q.shape
@@ -294,7 +295,31 @@ def e2e_pipelined(A, inp, steps, warmup):
     ms = start.elapsed_time(end) / steps
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = h_o.numel() * h_o.element_size() + h_l.numel() * h_l.element_size()
-    return ms, h2d, d2h
+
+    def copies(n):  # the step's copies without the attention
+        for _ in range(n):
+            ev = torch.cuda.Event()
+            ev.record(s_out)
+            s_in.wait_event(ev)
+            with torch.cuda.stream(s_in):
+                for d, h in zip(dev[0], host):
+                    d.copy_(h, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                h_o.copy_(outs[0][0], non_blocking=True)
+                h_l.copy_(outs[0][1], non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(s_in)
+            s_out.wait_event(done)
+
+    copies(2)
+    torch.cuda.synchronize()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(s_out)
+    copies(steps)
+    c1.record(s_out)
+    torch.cuda.synchronize()
+    return ms, h2d, d2h, c0.elapsed_time(c1) / steps
 
 
 def make_flush():
@@ -361,8 +386,11 @@ def run_ours(args, rank, world, local):
     # steps' attention (double-buffered device inputs and outputs): step k's
     # inputs travel while step k-1 computes, its outputs while step k+1 does.
     e2e_steps = max(3, args.steps // 2)
-    e2e_ms, h2d, d2h = e2e_pipelined(A, inp, e2e_steps, 2)
+    e2e_ms, h2d, d2h, link_ms = e2e_pipelined(A, inp, e2e_steps, 2)
     e2e_flops, e2e_ms_max = aggregate(flops, e2e_ms, world)
+    _, link_ms_max = aggregate(flops, link_ms, world)
+    e2e_value = e2e_flops / (e2e_ms_max * 1e-3) / 1e12
+    link_value = e2e_flops / (link_ms_max * 1e-3) / 1e12
 
     result = {
         "metric": "attn fwd TFLOPS (causal prefill, unmasked pairs) & % of GB300 bf16 tensor peak",
@@ -397,9 +425,14 @@ def run_ours(args, rank, world, local):
                      if pk_src == "measured" else "fallback 1.7 PFLOP/s sustained",
                      "kernel": kernel,
                      "algorithmic_flops_per_launch": flops},
-        "e2e": {"value": round(e2e_flops / (e2e_ms_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms_max, 4), "steps": e2e_steps,
+                "link_bound": {"ms_per_step": round(link_ms_max, 4), "value": round(link_value, 2),
+                               "frac": round(e2e_value / link_value, 4),
+                               "gbs": round((h2d + d2h) / (link_ms_max * 1e-3) / 1e9, 1),
+                               "note": "the step's copies alone, both directions at once: "
+                                       "the host link bounds a step at this"},
                 "pipeline": "copies on their own streams, overlapping the neighbouring steps' "
                             "attention (double-buffered device tensors); every step's inputs "
                             "go in and its outputs come out inside the timed region"},
@@ -607,6 +640,22 @@ def _extra_decode(A, inputs, pk, stream, flush, steps, warm, batch):
     return {key: e}
 
 
+# Special-function throughput of a GB300 SM (results per clock at the 2070 MHz
+# nominal clock; an event-timed probe of independent dependency chains):
+# ex2.approx 30.2, rcp.approx 15.3 (tanh.approx and lg2 15.3 too).
+SFU_PER_CLK = {"ex2": 30.2, "rcp": 15.3}
+SFU_CLOCK_HZ = 2.07e9
+
+
+def softcap_xu_peak_tflops(d, sms=152):
+    """Ceiling the special-function unit puts on a soft-capped prefill, in
+    TFLOP/s of the usual 4 d FLOP per kept score: each kept score needs two
+    ex2 (the tanh's 2^(2y log2 e) and the softmax's) and one rcp (the tanh's
+    1 / (e + 1))."""
+    sec_per_score = (2.0 / SFU_PER_CLK["ex2"] + 1.0 / SFU_PER_CLK["rcp"]) / (sms * SFU_CLOCK_HZ)
+    return 4.0 * d / sec_per_score / 1e12
+
+
 def _extra_varlen(A, inputs, pk, stream, flush, steps, warm):
     inp = inputs.workload(5, device="cuda")
     cq, ck = inp.cu_seqlens_q.cuda(), inp.cu_seqlens_k.cuda()
@@ -620,7 +669,13 @@ def _extra_varlen(A, inputs, pk, stream, flush, steps, warm):
         "value": round(fl / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
         "kernel": A.attn_last_kernel_name(),
         "roofline": {"bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}}}
+                     "frac": round(fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)},
+        "roofline_xu": {"bound": "xu", "peak": round(softcap_xu_peak_tflops(64), 1),
+                        "unit": "TFLOP/s",
+                        "frac": round(fl / (ms * 1e-3) / 1e12 / softcap_xu_peak_tflops(64), 4),
+                        "peak_source": "derived: 2 ex2 + 1 rcp per kept score at the special-"
+                                       "function rates of this GPU (probe: ex2 30.2, rcp 15.3 "
+                                       "results/clk/SM at 2070 MHz, 152 SMs)"}}}
 
 
 # ---------------------------------------------------------------------------
