@@ -87,7 +87,8 @@ EncodeTiledFn encode_fn() {
 // other dimensions have the given extents and byte strides, with the given
 // box.  dt: attn_dtype of the elements (e4m3 travels as bytes), or kMapF32.
 // Loads of Q/K/V use the 128-byte swizzle (one swizzle atom of 64 16-bit
-// elements per box row); the O store the 64-byte one; LSE none.
+// elements per box row); the O store the swizzle as wide as its box row (128
+// or 64 bytes); LSE none.
 constexpr int kMapF32 = -1;
 bool make_map(CUtensorMap* m, const void* base, int dt, int rank, const uint64_t* dims,
               const uint64_t* strides_bytes, const uint32_t* box,
